@@ -1,0 +1,404 @@
+#!/usr/bin/env python
+"""Benchmark of the W4A4 MoE expert layer (per-token NVFP4 activations,
+block-scaled grouped GEMMs on tcgen05) on GB300.
+
+A step is one pass of the whole path -- route, metadata, per-token
+quantization, permute, FC1 + SwiGLU + row amax, requant, FC2, weighted
+combine -- over one batch of the 32768-token Qwen3-30B-A3B-shaped layer
+(hidden 2048, 128 experts, top-8, FFN 768, router bias ~N(0, 2^2)), with
+seeded synthetic inputs resident in HBM and the weights quantized once
+before timing.  L2 is flushed (256 MiB write) between timed steps, outside
+the timed region; each step is timed with CUDA events on the launching
+stream, and per-stage events recorded by the library give the kernels'
+durations live.
+
+--gpus N runs N independent replicas (one process per GPU under torchrun):
+the layer is not sharded, nothing is exchanged on the data path; the only
+collectives are the barrier and the max over ranks of the timed region.
+--impl reference times the CPU oracle on a bounded sample of the same
+workload (rank 0 only).
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "MoE W4A4 expert-layer tokens/s"
+T, H, F, E, K_TOP = 32768, 2048, 768, 128, 8
+WORKLOAD = "moe_expert_layer_32k"
+CONFIG = {"workload": WORKLOAD, "tokens": T, "hidden": H, "ffn": F, "experts": E, "topk": K_TOP,
+          "router_bias_std": 2.0, "token_expert_rows": T * K_TOP, "weights": "pre-quantized NVFP4, static",
+          "l2": "flushed between timed steps (256 MiB write)", "seed": 3}
+FLUSH_BYTES = 256 << 20
+FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 : BF16 tensor rate
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--quick", action="store_true", help="profiling runs: no e2e, no oracle, no clocks")
+    return p.parse_args()
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available() and args.impl == "ours":
+        torch.cuda.set_device(local)
+    return rank, world, local
+
+
+def reduce_max(value, world, device):
+    """Max of a float over ranks (identity on one rank)."""
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.idx = device_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.reader.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- workload
+
+def make_inputs():
+    d = workloads.moe_32k()
+    return d
+
+
+def algorithmic(R):
+    """Per-launch algorithmic work of each stage (bytes or flops)."""
+    b16, f32 = 2, 4
+    q_row = H // 2 + H // 16 + f32
+    return {
+        "quantize": ("hbm", T * H * b16 + T * q_row),
+        "route": ("hbm", T * E * f32 + E * f32 + T * K_TOP * 8 + T * q_row + R * q_row + R * 8),
+        "fc1": ("tensor", 2.0 * R * (2 * F) * H),
+        "requant": ("hbm", R * F * b16 + R * f32 + R * (F // 2 + F // 16 + f32)),
+        "fc2": ("tensor", 2.0 * R * H * F),
+        "combine": ("hbm", R * H * b16 + T * K_TOP * 8 + T * H * b16),
+    }
+
+
+def run_ours(args, rank, world, local):
+    import nvfp4_quantized_moe_token_gb300 as nv
+    dev = torch.device("cuda", local)
+    peaks = {}
+    pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk):
+        with open(pk) as f:
+            peaks = json.load(f)
+    hbm_peak = peaks.get("hbm_gbs", 6800.0)
+    bf16_peak = peaks.get("bf16_tflops", 1900.0)
+    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+
+    d = make_inputs()
+    x = torch.from_numpy(d["x"].view(np.int16)).view(torch.bfloat16).to(dev)
+    logits = torch.from_numpy(d["logits"]).to(dev)
+    bias = torch.from_numpy(d["bias"]).to(dev)
+    w1q = nv.quantize_grouped_weights(torch.from_numpy(d["w1"].view(np.int16)).view(torch.bfloat16).to(dev))
+    w2q = nv.quantize_grouped_weights(torch.from_numpy(d["w2"].view(np.int16)).view(torch.bfloat16).to(dev))
+    need = nv.lib().moe_expert_workspace(T, H, F, E, K_TOP)
+    ws = torch.zeros(need, dtype=torch.uint8, device=dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    R = T * K_TOP
+
+    def step(evs=None):
+        nv.moe_expert_forward(x, logits, bias, w1q, w2q, F, K_TOP, out=out, ws=ws, stage_events=evs)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    err = ws[:4].view(torch.int32).item()
+    if err != 0:
+        raise RuntimeError(f"device error word {err:#x}")
+
+    clocks = ClockSampler(local) if not args.quick else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    nev = len(nv.STAGES) + 1
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        step(events[i])
+    torch.cuda.synchronize()
+    barrier(world)
+    step_ms = [ev[0].elapsed_time(ev[-1]) for ev in events]
+    stage_ms = {s: [ev[j].elapsed_time(ev[j + 1]) for ev in events] for j, s in enumerate(nv.STAGES)}
+    mean_ms = statistics.fmean(step_ms)
+    mean_ms_all = reduce_max(mean_ms, world, dev)
+
+    e2e = None
+    if not (args.no_e2e or args.quick):
+        xh = torch.from_numpy(d["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
+        lh = torch.from_numpy(d["logits"]).pin_memory()
+        bh = torch.from_numpy(d["bias"]).pin_memory()
+        oh = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+        xd, ld_, bd = torch.empty_like(x), torch.empty_like(logits), torch.empty_like(bias)
+
+        def e2e_step():
+            xd.copy_(xh, non_blocking=True)
+            ld_.copy_(lh, non_blocking=True)
+            bd.copy_(bh, non_blocking=True)
+            nv.moe_expert_forward(xd, ld_, bd, w1q, w2q, F, K_TOP, out=out, ws=ws)
+            oh.copy_(out, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(args.steps)]
+        barrier(world)
+        for a, b in pairs:
+            flush.zero_()
+            a.record(stream)
+            e2e_step()
+            b.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        e2e_ms = reduce_max(statistics.fmean(a.elapsed_time(b) for a, b in pairs), world, dev)
+        h2d = xh.numel() * 2 + lh.numel() * 4 + bh.numel() * 4
+        e2e = {"value": T * world / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": oh.numel() * 2}
+    clk = clocks.stop() if clocks else None
+
+    # per-stage rooflines, dominant stage first
+    alg = algorithmic(R)
+    stages = {}
+    for s in nv.STAGES:
+        ms = statistics.fmean(stage_ms[s])
+        bound, work = alg[s]
+        if bound == "tensor":
+            ach = work / (ms / 1e3) / 1e12
+            peak = bf16_peak * FP4_OVER_BF16
+            stages[s] = {"ms": ms, "share": ms / mean_ms, "bound": "tensor", "achieved": ach, "unit": "TFLOP/s",
+                         "peak": peak, "frac": ach / peak, "frac_of_9pf": ach / 9000.0,
+                         "frac_of_13_5pf": ach / 13500.0}
+        else:
+            ach = work / (ms / 1e3) / 1e9
+            stages[s] = {"ms": ms, "share": ms / mean_ms, "bound": "hbm", "achieved": ach, "unit": "GB/s",
+                         "peak": hbm_peak, "frac": ach / hbm_peak}
+    dom = max(stages, key=lambda s: stages[s]["ms"])
+    dm = stages[dom]
+    roofline = {"kernel": dom, "bound": dm["bound"], "achieved": dm["achieved"], "peak": dm["peak"],
+                "unit": dm["unit"], "frac": dm["frac"], "traffic": None,
+                "peak_source": f"{peak_src} ({'bf16 burst x 6 nominal FP4:BF16' if dm['bound'] == 'tensor' else 'copy GB/s'})",
+                "work_per_launch": alg[dom][1]}
+
+    res = {
+        "metric": METRIC, "value": T * world / (mean_ms_all / 1e3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms_all, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e2m1 x e4m3 -> f32 acc, bf16 io", "data": "synthetic",
+        "config": dict(CONFIG, parallelism=f"replicas x{world}"),
+        "e2e": e2e, "roofline": roofline, "stages": stages,
+        "gpu_launches": 8 * args.steps,
+        "clocks": clk,
+    }
+    return res, d
+
+
+def quant_gbs(args, local):
+    """Quantizer throughput on the 16384 x 2048 per-token workload (L2 flushed per rep)."""
+    import nvfp4_quantized_moe_token_gb300 as nv
+    dev = torch.device("cuda", local)
+    xb = workloads.quant_rows()["x"]
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).to(dev)
+    q = nv.NVFP4Tensor.empty(16384, 2048, 16384, dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(5):
+        nv.quantize_rows(x, out=q)
+    ts = []
+    for _ in range(50):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        nv.quantize_rows(x, out=q)
+        b.record()
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    ms = statistics.fmean(a.elapsed_time(b) for a, b in ts)
+    nbytes = 16384 * (2048 * 2 + 1024 + 128 + 4)
+    return {"workload": "quantize 16384 x 2048", "us": ms * 1e3, "gbs": nbytes / (ms / 1e3) / 1e9,
+            "algorithmic_bytes": nbytes}
+
+
+# ---------------------------------------------------------------- oracle timing
+
+def oracle_setup(d):
+    """Quantize and dequantize the static weights with the oracle (threads:
+    the C calls release the GIL)."""
+    import concurrent.futures as cf
+    import oracle
+
+    def one(e):
+        q1 = oracle.quantize(d["w1"][e], per_tensor=True)
+        q2 = oracle.quantize(d["w2"][e], per_tensor=True)
+        return q1, q2, oracle.dequantize(*q1, per_tensor=True), oracle.dequantize(*q2, per_tensor=True)
+
+    with cf.ThreadPoolExecutor(min(16, os.cpu_count() or 1)) as ex:
+        r = list(ex.map(one, range(E)))
+    return [x[0] for x in r], [x[1] for x in r], ([x[2] for x in r], [x[3] for x in r])
+
+
+def oracle_sample_tokens(d, w1q, w2q, wdeq, start, n):
+    import oracle
+    sl = slice(start, start + n)
+    oracle.moe_forward(d["x"][sl], d["logits"][sl], d["bias"], w1q, w2q, K_TOP, w_deq=wdeq)
+
+
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(d, budget_s=10.0, sample=64):
+    w1q, w2q, wdeq = oracle_setup(d)
+    n_tok, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < budget_s:
+        oracle_sample_tokens(d, w1q, w2q, wdeq, (n_tok * 7) % (T - sample), sample)
+        n_tok += sample
+    dt = time.perf_counter() - t0
+    return {"value": n_tok / dt, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+            "sample": f"{n_tok} tokens of the 32768-token layer in batches of {sample} "
+                      f"(full route/quantize/permute/FC1/SwiGLU/requant/FC2/combine per batch, fp64 GEMMs "
+                      f"via numpy BLAS, weights pre-quantized), {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    d = make_inputs()
+    w1q, w2q, wdeq = oracle_setup(d)
+    sample = 16
+    for i in range(args.warmup):
+        oracle_sample_tokens(d, w1q, w2q, wdeq, i * sample, sample)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle_sample_tokens(d, w1q, w2q, wdeq, (i * sample * 13) % (T - sample), sample)
+    dt = time.perf_counter() - t0
+    value = args.steps * sample / dt
+    res = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+           "data": "synthetic", "config": dict(CONFIG, parallelism="host cores"),
+           "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+                            "sample": f"each step: {sample} tokens of the 32768-token layer through the CPU "
+                                      f"oracle (weights pre-quantized)"},
+           "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res))
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    import nvfp4_quantized_moe_token_gb300 as nv
+    nv.lib()
+    res, d = run_ours(args, rank, world, local)
+    if rank == 0:
+        if not args.quick:
+            res["quant"] = quant_gbs(args, local)
+        if not (args.no_cpu_baseline or args.quick):
+            res["cpu_baseline"] = cpu_baseline(d)
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,242 @@
+/*
+ * nvfp4moe.h -- C ABI of the per-token NVFP4 W4A4 forward path for GB300 (sm_103a).
+ *
+ * Three compute calls, following the problem statement of the pages:
+ *   nvfp4_quantize_rows  bf16 rows -> packed E2M1 codes, one E4M3 scale per
+ *                        16-element block (in the swizzled layout that block-
+ *                        scaled tensor-core MMA reads), one fp32 scale per row
+ *                        (activations) or per tensor (weights).
+ *   nvfp4_linear         dense W4A4 GEMM Y = bf16(deq(X) . deq(W)^T).
+ *   moe_expert_forward   route -> permute by expert -> FC1 gate/up -> SwiGLU
+ *                        -> requant -> FC2 -> router-weighted combine.
+ *
+ * Sources (page title, section):
+ *   "miniTE Technical Report: Stable and Efficient Reinforcement Learning
+ *   with Native NVFP4": 2.2 (x^ = q s_b s_g), 2.3 and 5.1 (per-token outer
+ *   scale), 5.2 (contiguous quantized buffers, device-side expert offsets,
+ *   zero-token experts and padding in one grouped path, workspace reuse),
+ *   5.3 (amax computed where data are produced and reused by the quantizer),
+ *   5.4 (block-scaled GEMM epilogue ACC x alpha_a[m] x alpha_b, C = gate|up,
+ *   D = act(gate, up), concurrent amax of D), 5.6 (gs = gamax / 2688, zero
+ *   rows give zero).
+ *   "The 4-bitter Lesson": baseline recipe (per-token activation scale fused
+ *   into the quantization kernel; weights with one fp32 scale per tensor).
+ *
+ * Conventions for every call:
+ *   - All buffers are DEVICE memory allocated and owned by the caller.  The
+ *     library never allocates, frees, synchronizes or copies to the host.
+ *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL is
+ *     the legacy default stream) and completes asynchronously.
+ *   - Return value 0 = enqueued; negative = rejected before any launch
+ *     (nothing was written), or a launch error:
+ *       NVFP4_EINVAL  -1  null pointer / bad enum / negative size
+ *       NVFP4_ESHAPE  -2  unsupported shape (see each call)
+ *       NVFP4_EALIGN  -3  misaligned pointer or leading dimension
+ *       NVFP4_EWORKSPACE -4 workspace too small
+ *       NVFP4_ELAUNCH -5  CUDA error while enqueueing
+ *     nvfp4_last_error() returns a message for the last failure on the
+ *     calling thread.
+ *   - Inputs must be finite; NaN/Inf inputs are outside the contract.
+ *   - Device-side faults are never raised on purpose: a kernel that detects
+ *     an inconsistency (or a pipeline wait that exceeds its time limit)
+ *     ORs a bit into a device error word and returns.  The error word is
+ *     the first uint32 of `ws` for nvfp4_linear (when ws_bytes >= 4) and
+ *     the `err` slot of moe_expert_forward's workspace.  The library never
+ *     clears it: the caller zeroes it and reads it when convenient.
+ */
+#ifndef NVFP4MOE_H
+#define NVFP4MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define NVFP4_API __attribute__((visibility("default")))
+#else
+#define NVFP4_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define NVFP4_OK 0
+#define NVFP4_EINVAL (-1)
+#define NVFP4_ESHAPE (-2)
+#define NVFP4_EALIGN (-3)
+#define NVFP4_EWORKSPACE (-4)
+#define NVFP4_ELAUNCH (-5)
+
+/* Scale modes of nvfp4_quantize_rows. */
+#define NVFP4_PER_ROW 0    /* one fp32 outer scale per row (per token) */
+#define NVFP4_PER_TENSOR 1 /* one fp32 outer scale for the whole matrix */
+
+/* Bits of the device error word. */
+#define NVFP4_DEVERR_TIMEOUT 1u   /* a pipeline wait in the GEMM ran past its limit */
+#define NVFP4_DEVERR_BADEXPERT 2u /* a routed expert id outside [0, E) */
+
+/*
+ * An NVFP4 matrix [rows x cols] in device memory (caller-owned):
+ *   codes  uint8 [rows x cols/2]: E2M1 codes, row-major, element 2i of a row
+ *          in the low nibble of byte i, element 2i+1 in the high nibble;
+ *          code = sign bit (8) | index into {0, .5, 1, 1.5, 2, 3, 4, 6}.
+ *   sf     E4M3 block scales, nvfp4_sf_bytes(rows, cols) bytes, swizzled:
+ *          the [rows x cols/16] scale matrix padded to 128-row x 4-column
+ *          tiles of 512 bytes, tiles of one 128-row band consecutive, and
+ *          inside a tile byte (r, c) at (r%32)*16 + ((r%128)/32)*4 + c%4.
+ *   scale  fp32 outer scales s_g: [rows] (per row) or [1] (per tensor).
+ * Decoding: x^[r][j] = E2M1(code) * E4M3(sf block) * s_g.
+ */
+typedef struct nvfp4_tensor {
+    uint8_t* codes;
+    uint8_t* sf;
+    float* scale;
+    int64_t rows;
+    int64_t cols;
+} nvfp4_tensor;
+
+/* Bytes of the swizzled block-scale buffer of a [rows x cols] matrix:
+ * ceil(rows/128)*128 * ceil(cols/64)*4.  Pure host function. */
+NVFP4_API size_t nvfp4_sf_bytes(int64_t rows, int64_t cols);
+
+/* Workspace bytes nvfp4_quantize_rows needs: 0 for NVFP4_PER_ROW or when
+ * amax_in is given, 256 for NVFP4_PER_TENSOR without amax_in (the tensor
+ * amax is reduced there).  Pure host function. */
+NVFP4_API size_t nvfp4_quantize_workspace(int64_t rows, int64_t cols, int scale_mode);
+
+/*
+ * nvfp4_quantize_rows: quantize a bf16 matrix x [rows x cols] (row stride
+ * ld elements) to NVFP4 into `out` (out->rows/cols must equal rows/cols).
+ *
+ * Per row ("miniTE Technical Report" 5.1, 5.6; "The 4-bitter Lesson"):
+ *   amax = max_j |x_j| over the row (NVFP4_PER_ROW) or the whole matrix
+ *          (NVFP4_PER_TENSOR); amax_in (nullable, device) replaces the
+ *          reduction: [rows] values for per-row, [1] for per-tensor
+ *          ("miniTE Technical Report" 5.3: the producer's amax is reused).
+ *   s_g  = amax / 2688 (fp32); s_g == 0 -> the row is all-zero codes/scales.
+ *   per 16-block: s_b = E4M3_rne_satfinite(bmax / (6 s_g)); s_b == 0 ->
+ *          codes 0; else d = s_b s_g and v = x * (1/d) (v = x / d if d is
+ *          an fp32 subnormal); code = E2M1_rne_saturating(v), sign kept.
+ * Every step is an IEEE fp32 operation in that order, so the result is
+ * bit-identical to any implementation of the same steps.
+ * Shapes: rows >= 0, cols > 0, cols % 16 == 0, ld >= cols.
+ * Alignment: x and ld*2 bytes 16-byte aligned; codes 16-byte aligned.
+ * Scale-factor padding rows/columns (beyond rows or cols/16) are not written.
+ * ws: nvfp4_quantize_workspace() bytes (may be NULL when that is 0).
+ */
+NVFP4_API int nvfp4_quantize_rows(const void* x_bf16, int64_t rows, int64_t cols, int64_t ld,
+                        int scale_mode, const float* amax_in, const nvfp4_tensor* out,
+                        void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * nvfp4_linear: y[m][n] = bf16( s_gx[m] * s_gw * sum_k (q_x s_bx)(q_w s_bw) )
+ * for x [M x K] quantized per row and w [N x K] (K-major, i.e. the weight
+ * transposed) quantized per tensor.  Accumulation is fp32 on the tensor
+ * cores ("miniTE Technical Report" 5.4: ACC x alpha_a[m] x alpha_b; 5.2
+ * dense path).  y is bf16 [M x N] with row stride ldy elements.
+ * Shapes: K % 64 == 0, N % 256 == 0, M >= 0, ldy >= N, ldy % 8 == 0.
+ * Alignment: codes and sf 16-byte aligned, y 16-byte aligned.
+ * ws: nullable; when ws_bytes >= 4 its first uint32 is the device error word.
+ */
+NVFP4_API int nvfp4_linear(const nvfp4_tensor* x, const nvfp4_tensor* w, void* y_bf16, int64_t ldy,
+                 void* ws, size_t ws_bytes, void* stream);
+
+/* Options of moe_expert_forward. */
+typedef struct moe_options {
+    /* 0: router weight applied in the combine (default).  1: applied to
+     * the SwiGLU output before the FC2 amax / quantization ("miniTE
+     * Technical Report" 5.3 weighted SwiGLU; the combine then sums the
+     * expert outputs unweighted). */
+    int weight_at_fc1;
+} moe_options;
+
+/* Optional debug outputs of moe_expert_forward (all nullable, device). */
+typedef struct moe_debug {
+    /* fp32 [R x 2F], R = T*topk rows in expert order: the FC1 output after
+     * the alpha scaling, before SwiGLU (gate columns then up columns). */
+    float* fc1_out;
+    /* MOE_STAGE_EVENTS cudaEvent_t handles (created by the caller) recorded
+     * on `stream` before the first stage and after each stage: quantize X,
+     * route + permute, FC1, requant, FC2, combine. */
+    void** stage_events;
+} moe_debug;
+
+#define MOE_STAGE_EVENTS 7
+
+/*
+ * Offsets (bytes from the workspace base) of the intermediates that
+ * moe_expert_forward leaves in its workspace, for inspection after the
+ * call completes.  R = T*topk token-expert rows, Rp = padded row bound.
+ */
+typedef struct moe_workspace_layout {
+    size_t total;        /* workspace bytes required */
+    size_t err;          /* uint32 device error word (+ scratch words) */
+    size_t ids;          /* int32 [T x topk] routed expert ids, descending z */
+    size_t weights;      /* fp32 [T x topk] router weights (softmax over the selected) */
+    size_t row_weights;  /* fp32 [R] router weight of each expert-ordered row (weight_at_fc1 only) */
+    size_t counts;       /* int32 [E] rows per expert */
+    size_t offsets;      /* int32 [E+1] exclusive prefix of counts */
+    size_t padded_offsets; /* int32 [E+1] prefix of ceil(count/128)*128 */
+    size_t perm;         /* int32 [R] t*topk+slot of each expert-ordered row */
+    size_t inv;          /* int32 [T x topk] expert-ordered row of (t, slot) */
+    size_t chunk_counts; /* int32 scratch for the stable scatter */
+    size_t xq_codes;     /* uint8 [T x H/2] per-token quantized X */
+    size_t xq_sf;        /* swizzled [T x H/16] */
+    size_t xq_scale;     /* fp32 [T] */
+    size_t a1_codes;     /* uint8 [R x H/2] X rows in expert order */
+    size_t a1_sf;        /* swizzled, expert e's rows start at padded row padded_offsets[e] */
+    size_t a1_scale;     /* fp32 [R] */
+    size_t d;            /* bf16 [R x F] SwiGLU output */
+    size_t amax2;        /* fp32 [R] row amax of d (from the FC1 epilogue) */
+    size_t a2_codes;     /* uint8 [R x F/2] requantized d */
+    size_t a2_sf;        /* swizzled [Rp x F/16], padded per expert like a1_sf */
+    size_t a2_scale;     /* fp32 [R] */
+    size_t y2;           /* bf16 [R x H] FC2 output in expert order */
+} moe_workspace_layout;
+
+/* Fill *layout for the given sizes; returns 0, or NVFP4_ESHAPE /
+ * NVFP4_EINVAL for sizes moe_expert_forward rejects.  Pure host function. */
+NVFP4_API int moe_expert_workspace_layout(int64_t T, int64_t H, int64_t F, int E, int topk,
+                                moe_workspace_layout* layout);
+
+/* Workspace bytes moe_expert_forward needs (0 for rejected sizes). */
+NVFP4_API size_t moe_expert_workspace(int64_t T, int64_t H, int64_t F, int E, int topk);
+
+/*
+ * moe_expert_forward: one MoE expert layer, W4A4 forward, all on device.
+ *   x              bf16 [T x H] token activations (row stride H)
+ *   router_logits  fp32 [T x E]; router_bias fp32 [E] (nullable = zeros)
+ *   w1             E experts stacked: rows = E*2F, cols = H; expert e owns
+ *                  rows [e*2F, (e+1)*2F) = gate (F rows) then up (F rows);
+ *                  scale = fp32 [E], one per-tensor scale per expert
+ *   w2             rows = E*H, cols = F; expert e owns rows [e*H, (e+1)*H);
+ *                  scale = fp32 [E]
+ *   out            bf16 [T x H]
+ * Steps: z = logit + bias; top-k of z (ties to the lower expert), weights =
+ * softmax over the k selected z; expert histogram, offsets and a stable
+ * (expert, token) permutation built on the device; X quantized once per
+ * token and its rows gathered into expert order; FC1 grouped block-scaled
+ * GEMM with the SwiGLU + row-amax epilogue writing bf16 D; D requantized per
+ * row with the reused amax; FC2 grouped GEMM writing bf16 Y2; out[t] =
+ * bf16( sum_slot w[t,slot] * Y2[row(t,slot)] ) accumulated in fp32 in slot
+ * order.  No host synchronization anywhere.
+ * Shapes: T >= 1, H % 256 == 0, F % 128 == 0, 1 <= topk <= min(E, 16),
+ *         E % 32 == 0, 32 <= E <= 256.
+ * Alignment: every pointer 16-byte aligned; ws 256-byte aligned.
+ * ws: moe_expert_workspace() bytes; its intermediates are described by
+ * moe_expert_workspace_layout().  opt and dbg are nullable.
+ */
+NVFP4_API int moe_expert_forward(const void* x_bf16, int64_t T, int64_t H,
+                       const float* router_logits, const float* router_bias, int E, int topk,
+                       const nvfp4_tensor* w1, const nvfp4_tensor* w2, int64_t F,
+                       const moe_options* opt, void* out_bf16, const moe_debug* dbg,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* Message describing the last error returned on the calling thread ("" if none). */
+NVFP4_API const char* nvfp4_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4MOE_H */

@@ -1,0 +1,224 @@
+"""Python binding of libnvfp4moe.so (include/nvfp4moe.h): argument marshalling only.
+
+Every step of the path runs in the library's sm_103a kernels; this module
+only allocates device buffers with torch, passes raw pointers and the
+current CUDA stream, and turns nonzero return codes into exceptions.  There
+is no fallback: if the shared library is missing or a GPU is absent the
+calls raise.
+"""
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB = None
+
+c_i64 = ctypes.c_int64
+c_vp = ctypes.c_void_p
+
+
+class _Tensor(ctypes.Structure):
+    _fields_ = [("codes", c_vp), ("sf", c_vp), ("scale", c_vp), ("rows", c_i64), ("cols", c_i64)]
+
+
+class _Options(ctypes.Structure):
+    _fields_ = [("weight_at_fc1", ctypes.c_int)]
+
+
+class _Debug(ctypes.Structure):
+    _fields_ = [("fc1_out", c_vp), ("stage_events", ctypes.POINTER(c_vp))]
+
+
+STAGES = ["quantize", "route", "fc1", "requant", "fc2", "combine"]
+
+
+LAYOUT_FIELDS = ["total", "err", "ids", "weights", "row_weights", "counts", "offsets", "padded_offsets",
+                 "perm", "inv", "chunk_counts", "xq_codes", "xq_sf", "xq_scale", "a1_codes", "a1_sf",
+                 "a1_scale", "d", "amax2", "a2_codes", "a2_sf", "a2_scale", "y2"]
+
+
+class _Layout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in LAYOUT_FIELDS]
+
+
+PER_ROW = 0
+PER_TENSOR = 1
+SYMBOLS = ["nvfp4_sf_bytes", "nvfp4_quantize_workspace", "nvfp4_quantize_rows", "nvfp4_linear",
+           "moe_expert_workspace_layout", "moe_expert_workspace", "moe_expert_forward",
+           "nvfp4_last_error"]
+
+
+class NVFP4Error(RuntimeError):
+    pass
+
+
+def library_path():
+    return _build.LIB
+
+
+def lib():
+    """Load the shared library (built in-tree by build.build())."""
+    global _LIB
+    if _LIB is None:
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise NVFP4Error(f"{path} is missing: run __graft_entry__.build() (or "
+                             "nvfp4_quantized_moe_token_gb300.build.build()) first")
+        L = ctypes.CDLL(path)
+        L.nvfp4_sf_bytes.restype = ctypes.c_size_t
+        L.nvfp4_sf_bytes.argtypes = [c_i64, c_i64]
+        L.nvfp4_quantize_workspace.restype = ctypes.c_size_t
+        L.nvfp4_quantize_workspace.argtypes = [c_i64, c_i64, ctypes.c_int]
+        L.nvfp4_quantize_rows.restype = ctypes.c_int
+        L.nvfp4_quantize_rows.argtypes = [c_vp, c_i64, c_i64, c_i64, ctypes.c_int, c_vp,
+                                          ctypes.POINTER(_Tensor), c_vp, ctypes.c_size_t, c_vp]
+        L.nvfp4_linear.restype = ctypes.c_int
+        L.nvfp4_linear.argtypes = [ctypes.POINTER(_Tensor), ctypes.POINTER(_Tensor), c_vp, c_i64,
+                                   c_vp, ctypes.c_size_t, c_vp]
+        L.moe_expert_workspace_layout.restype = ctypes.c_int
+        L.moe_expert_workspace_layout.argtypes = [c_i64, c_i64, c_i64, ctypes.c_int, ctypes.c_int,
+                                                  ctypes.POINTER(_Layout)]
+        L.moe_expert_workspace.restype = ctypes.c_size_t
+        L.moe_expert_workspace.argtypes = [c_i64, c_i64, c_i64, ctypes.c_int, ctypes.c_int]
+        L.moe_expert_forward.restype = ctypes.c_int
+        L.moe_expert_forward.argtypes = [c_vp, c_i64, c_i64, c_vp, c_vp, ctypes.c_int, ctypes.c_int,
+                                         ctypes.POINTER(_Tensor), ctypes.POINTER(_Tensor), c_i64,
+                                         ctypes.POINTER(_Options), c_vp, ctypes.POINTER(_Debug),
+                                         c_vp, ctypes.c_size_t, c_vp]
+        L.nvfp4_last_error.restype = ctypes.c_char_p
+        L.nvfp4_last_error.argtypes = []
+        _LIB = L
+    return _LIB
+
+
+def _check(rc, what):
+    if rc != 0:
+        msg = lib().nvfp4_last_error().decode()
+        raise NVFP4Error(f"{what} failed ({rc}): {msg}")
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+class NVFP4Tensor:
+    """An NVFP4 matrix on the device: packed E2M1 codes [rows, cols/2],
+    swizzled E4M3 block scales (sf_bytes(rows, cols) bytes) and fp32 outer
+    scales ([rows], [1] or one per stacked group)."""
+
+    def __init__(self, codes, sf, scale, rows, cols):
+        self.codes, self.sf, self.scale = codes, sf, scale
+        self.rows, self.cols = int(rows), int(cols)
+
+    @classmethod
+    def empty(cls, rows, cols, n_scales, device="cuda"):
+        codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=device)
+        sf = torch.empty(max(sf_bytes(rows, cols), 16), dtype=torch.uint8, device=device)
+        scale = torch.empty(max(n_scales, 1), dtype=torch.float32, device=device)
+        return cls(codes, sf, scale, rows, cols)
+
+    def c(self):
+        return _Tensor(self.codes.data_ptr(), self.sf.data_ptr(), self.scale.data_ptr(),
+                       self.rows, self.cols)
+
+
+def sf_bytes(rows, cols):
+    return int(lib().nvfp4_sf_bytes(rows, cols))
+
+
+def quantize_rows(x, per_tensor=False, amax_in=None, out=None, stream=None):
+    """bf16 [rows, cols] (CUDA) -> NVFP4Tensor (per-row or per-tensor outer scale)."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    rows, cols = x.shape
+    if out is None:
+        out = NVFP4Tensor.empty(rows, cols, 1 if per_tensor else rows, x.device)
+    mode = PER_TENSOR if per_tensor else PER_ROW
+    ws_bytes = int(lib().nvfp4_quantize_workspace(rows, cols, mode))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=x.device) if ws_bytes else None
+    t = out.c()
+    rc = lib().nvfp4_quantize_rows(_ptr(x), rows, cols, x.stride(0), mode, _ptr(amax_in), ctypes.byref(t),
+                                   _ptr(ws), ws_bytes, _stream(stream))
+    _check(rc, "nvfp4_quantize_rows")
+    return out
+
+
+def quantize_grouped_weights(w, stream=None):
+    """Per-expert weights bf16 [G, N, K] -> one stacked NVFP4Tensor [G*N, K]
+    with one per-tensor scale per expert (scale has G entries).  Requires
+    N % 128 == 0 so each expert's swizzled scales are a contiguous slice."""
+    G, N, K = w.shape
+    assert N % 128 == 0
+    out = NVFP4Tensor.empty(G * N, K, G, w.device)
+    per_sf = sf_bytes(N, K)
+    ws = torch.empty(256, dtype=torch.uint8, device=w.device)
+    for g in range(G):
+        sub = _Tensor(out.codes.data_ptr() + g * N * (K // 2), out.sf.data_ptr() + g * per_sf,
+                      out.scale.data_ptr() + 4 * g, N, K)
+        rc = lib().nvfp4_quantize_rows(_ptr(w[g]), N, K, K, PER_TENSOR, None, ctypes.byref(sub),
+                                       _ptr(ws), 256, _stream(stream))
+        _check(rc, "nvfp4_quantize_rows (weights)")
+    return out
+
+
+def linear(xq, wq, out=None, err=None, stream=None):
+    """y = bf16( deq(x) . deq(w)^T ): x per-row, w per-tensor (K-major [N, K])."""
+    M, N = xq.rows, wq.rows
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=xq.codes.device)
+    a, b = xq.c(), wq.c()
+    rc = lib().nvfp4_linear(ctypes.byref(a), ctypes.byref(b), _ptr(out), out.stride(0),
+                            _ptr(err), 0 if err is None else err.numel() * err.element_size(),
+                            _stream(stream))
+    _check(rc, "nvfp4_linear")
+    return out
+
+
+def moe_workspace_layout(T, H, F, E, topk):
+    L = _Layout()
+    _check(lib().moe_expert_workspace_layout(T, H, F, E, topk, ctypes.byref(L)), "moe_expert_workspace_layout")
+    return {n: int(getattr(L, n)) for n in LAYOUT_FIELDS}
+
+
+def moe_expert_forward(x, logits, bias, w1q, w2q, F, topk, weight_at_fc1=False, out=None,
+                       ws=None, fc1_debug=None, stage_events=None, stream=None):
+    """One W4A4 MoE expert layer on the device.  Returns (out bf16 [T, H], ws).
+
+    stage_events (optional): len(STAGES) + 1 torch.cuda.Event objects recorded on
+    the stream before the first stage and after each stage."""
+    T, H = x.shape
+    E = logits.shape[1]
+    need = int(lib().moe_expert_workspace(T, H, F, E, topk))
+    if ws is None:
+        ws = torch.empty(need, dtype=torch.uint8, device=x.device)
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    a, b = w1q.c(), w2q.c()
+    opt = _Options(1 if weight_at_fc1 else 0)
+    evs = None
+    if stage_events is not None:
+        assert len(stage_events) == len(STAGES) + 1
+        evs = (c_vp * len(stage_events))(*[e.cuda_event for e in stage_events])
+    dbg = _Debug(None if fc1_debug is None else fc1_debug.data_ptr(), evs)
+    rc = lib().moe_expert_forward(_ptr(x), T, H, _ptr(logits), _ptr(bias), E, topk, ctypes.byref(a),
+                                  ctypes.byref(b), F, ctypes.byref(opt), _ptr(out), ctypes.byref(dbg),
+                                  _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "moe_expert_forward")
+    return out, ws
+
+
+def ws_view(ws, layout, field, dtype, shape):
+    """A typed view of one intermediate inside the MoE workspace."""
+    off = layout[field]
+    n = 1
+    for s in shape:
+        n *= s
+    nbytes = n * torch.empty(0, dtype=dtype).element_size()
+    return ws[off:off + nbytes].view(dtype).view(*shape)

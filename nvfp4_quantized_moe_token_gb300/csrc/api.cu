@@ -1,0 +1,359 @@
+// api.cu -- the C ABI (include/nvfp4moe.h): argument validation, workspace
+// layout and the launch sequence of each call.  No allocation, no host
+// synchronization, no device-to-host copy.
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <string>
+
+#include "../../include/nvfp4moe.h"
+#include "kernels.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+
+int ok() {
+    g_last_error.clear();
+    return NVFP4_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int64_t sf_bytes_of(int64_t rows, int64_t cols) {
+    return (rows + 127) / 128 * 128 * ((cols / 16 + 3) / 4 * 4);
+}
+
+int sm_count() {
+    static int n = 0;
+    if (n == 0) n = nvfp4::device_sm_count();
+    return n;
+}
+
+int check_tensor(const nvfp4_tensor* t, const char* name) {
+    if (t == nullptr || t->codes == nullptr || t->sf == nullptr || t->scale == nullptr)
+        return fail(NVFP4_EINVAL, "%s: null tensor or buffer", name);
+    if (!aligned(t->codes, 16) || !aligned(t->sf, 16) || !aligned(t->scale, 4))
+        return fail(NVFP4_EALIGN, "%s: codes/sf must be 16-byte aligned, scale 4-byte aligned", name);
+    if (t->rows < 0 || t->cols <= 0) return fail(NVFP4_EINVAL, "%s: bad size %lld x %lld", name,
+                                                 (long long)t->rows, (long long)t->cols);
+    return NVFP4_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* nvfp4_last_error(void) { return g_last_error.c_str(); }
+
+size_t nvfp4_sf_bytes(int64_t rows, int64_t cols) {
+    if (rows < 0 || cols < 0) return 0;
+    return (size_t)sf_bytes_of(rows, cols);
+}
+
+size_t nvfp4_quantize_workspace(int64_t rows, int64_t cols, int scale_mode) {
+    (void)rows;
+    (void)cols;
+    return scale_mode == NVFP4_PER_TENSOR ? 256 : 0;
+}
+
+int nvfp4_quantize_rows(const void* x_bf16, int64_t rows, int64_t cols, int64_t ld, int scale_mode,
+                        const float* amax_in, const nvfp4_tensor* out, void* ws, size_t ws_bytes,
+                        void* stream) {
+    if (x_bf16 == nullptr) return fail(NVFP4_EINVAL, "quantize: x is null");
+    if (scale_mode != NVFP4_PER_ROW && scale_mode != NVFP4_PER_TENSOR)
+        return fail(NVFP4_EINVAL, "quantize: unknown scale_mode %d", scale_mode);
+    int rc = check_tensor(out, "quantize out");
+    if (rc) return rc;
+    if (rows < 0 || cols <= 0 || ld < cols) return fail(NVFP4_EINVAL, "quantize: bad rows/cols/ld");
+    if (out->rows != rows || out->cols != cols) return fail(NVFP4_EINVAL, "quantize: out shape mismatch");
+    if (cols % 16 != 0) return fail(NVFP4_ESHAPE, "quantize: cols %% 16 != 0 (cols = %lld)", (long long)cols);
+    if (rows >= (1ll << 31) || cols >= (1ll << 24)) return fail(NVFP4_ESHAPE, "quantize: matrix too large");
+    if (!aligned(x_bf16, 16) || (ld % 8) != 0) return fail(NVFP4_EALIGN, "quantize: x and ld*2 must be 16-byte aligned");
+    if (amax_in != nullptr && !aligned(amax_in, 4)) return fail(NVFP4_EALIGN, "quantize: amax_in misaligned");
+    if (scale_mode == NVFP4_PER_TENSOR && amax_in == nullptr) {
+        if (ws == nullptr || ws_bytes < 256) return fail(NVFP4_EWORKSPACE, "quantize: per-tensor needs 256 bytes of ws");
+        if (!aligned(ws, 16)) return fail(NVFP4_EALIGN, "quantize: ws must be 16-byte aligned");
+    }
+    nvfp4::QuantLaunch q{};
+    q.x = x_bf16;
+    q.ld = ld;
+    q.rows = rows;
+    q.cols = cols;
+    q.amax_in = amax_in;
+    q.per_tensor = scale_mode == NVFP4_PER_TENSOR;
+    q.codes = out->codes;
+    q.sf = out->sf;
+    q.scale = out->scale;
+    q.ws = ws;
+    cudaError_t e = nvfp4::launch_quantize(q, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(NVFP4_ELAUNCH, "quantize: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+int nvfp4_linear(const nvfp4_tensor* x, const nvfp4_tensor* w, void* y_bf16, int64_t ldy, void* ws,
+                 size_t ws_bytes, void* stream) {
+    int rc = check_tensor(x, "linear x");
+    if (rc) return rc;
+    rc = check_tensor(w, "linear w");
+    if (rc) return rc;
+    if (y_bf16 == nullptr) return fail(NVFP4_EINVAL, "linear: y is null");
+    const int64_t M = x->rows, K = x->cols, N = w->rows;
+    if (w->cols != K) return fail(NVFP4_EINVAL, "linear: x cols %lld != w cols %lld", (long long)K, (long long)w->cols);
+    if (K % 64 != 0) return fail(NVFP4_ESHAPE, "linear: K %% 64 != 0 (K = %lld)", (long long)K);
+    if (N <= 0 || N % 256 != 0) return fail(NVFP4_ESHAPE, "linear: N %% 256 != 0 (N = %lld)", (long long)N);
+    if (M >= (1ll << 31) || N >= (1ll << 31) || K >= (1ll << 24)) return fail(NVFP4_ESHAPE, "linear: too large");
+    if (ldy < N || ldy % 8 != 0) return fail(NVFP4_EALIGN, "linear: ldy must be >= N and a multiple of 8");
+    if (!aligned(y_bf16, 16)) return fail(NVFP4_EALIGN, "linear: y must be 16-byte aligned");
+    if (ws != nullptr && ws_bytes >= 4 && !aligned(ws, 4)) return fail(NVFP4_EALIGN, "linear: ws misaligned");
+    if (sm_count() <= 0) return fail(NVFP4_ELAUNCH, "linear: no CUDA device");
+    nvfp4::GemmLaunch g{};
+    g.a_codes = x->codes;
+    g.a_sf = x->sf;
+    g.a_scale = x->scale;
+    g.M = M;
+    g.b_codes = w->codes;
+    g.b_sf = w->sf;
+    g.b_scale = w->scale;
+    g.N = (int)N;
+    g.K = (int)K;
+    g.G = 1;
+    g.goff = nullptr;
+    g.gpoff = nullptr;
+    g.mode = 0;
+    g.out = y_bf16;
+    g.ldo = ldy;
+    g.err = (ws != nullptr && ws_bytes >= 4) ? reinterpret_cast<uint32_t*>(ws) : nullptr;
+    g.num_sms = sm_count();
+    cudaError_t e = nvfp4::launch_gemm(g, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(NVFP4_ELAUNCH, "linear: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+static int moe_check_sizes(int64_t T, int64_t H, int64_t F, int E, int topk) {
+    if (T < 1) return fail(NVFP4_EINVAL, "moe: T must be >= 1");
+    if (H <= 0 || H % 256 != 0) return fail(NVFP4_ESHAPE, "moe: H %% 256 != 0 (H = %lld)", (long long)H);
+    if (F <= 0 || F % 128 != 0) return fail(NVFP4_ESHAPE, "moe: F %% 128 != 0 (F = %lld)", (long long)F);
+    if (E < 32 || E > 256 || E % 32 != 0) return fail(NVFP4_ESHAPE, "moe: E must be a multiple of 32 in [32, 256]");
+    if (topk < 1 || topk > 16 || topk > E) return fail(NVFP4_ESHAPE, "moe: topk must be in [1, min(E, 16)]");
+    if (T * topk >= (1ll << 30) || H >= (1 << 16) || F >= (1 << 16))
+        return fail(NVFP4_ESHAPE, "moe: sizes too large");
+    return NVFP4_OK;
+}
+
+int moe_expert_workspace_layout(int64_t T, int64_t H, int64_t F, int E, int topk, moe_workspace_layout* L) {
+    if (L == nullptr) return fail(NVFP4_EINVAL, "moe layout: null");
+    int rc = moe_check_sizes(T, H, F, E, topk);
+    if (rc) return rc;
+    const int64_t R = T * topk;
+    const int64_t Rp = (R + 127 * (int64_t)E + 127) / 128 * 128;
+    const int64_t nchunks = (T + nvfp4::kRouteChunk - 1) / nvfp4::kRouteChunk;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = o;
+        o = align_up(o + bytes, 256);
+        return at;
+    };
+    L->err = take(256);
+    L->ids = take(4 * R);
+    L->weights = take(4 * R);
+    L->row_weights = take(4 * R);
+    L->counts = take(4 * E);
+    L->offsets = take(4 * (E + 1));
+    L->padded_offsets = take(4 * (E + 1));
+    L->perm = take(4 * R);
+    L->inv = take(4 * R);
+    L->chunk_counts = take(2 * 4 * nchunks * E);
+    L->xq_codes = take(T * H / 2);
+    L->xq_sf = take(sf_bytes_of(T, H));
+    L->xq_scale = take(4 * T);
+    L->a1_codes = take(R * H / 2);
+    L->a1_sf = take(Rp * H / 16);
+    L->a1_scale = take(4 * R);
+    L->d = take(2 * R * F);
+    L->amax2 = take(4 * R);
+    L->a2_codes = take(R * F / 2);
+    L->a2_sf = take(Rp * ((F / 16 + 3) / 4 * 4));
+    L->a2_scale = take(4 * R);
+    L->y2 = take(2 * R * H);
+    L->total = o;
+    return ok();
+}
+
+size_t moe_expert_workspace(int64_t T, int64_t H, int64_t F, int E, int topk) {
+    moe_workspace_layout L;
+    return moe_expert_workspace_layout(T, H, F, E, topk, &L) == NVFP4_OK ? L.total : 0;
+}
+
+int moe_expert_forward(const void* x_bf16, int64_t T, int64_t H, const float* router_logits,
+                       const float* router_bias, int E, int topk, const nvfp4_tensor* w1,
+                       const nvfp4_tensor* w2, int64_t F, const moe_options* opt, void* out_bf16,
+                       const moe_debug* dbg, void* ws, size_t ws_bytes, void* stream) {
+    moe_workspace_layout L;
+    int rc = moe_expert_workspace_layout(T, H, F, E, topk, &L);
+    if (rc) return rc;
+    if (x_bf16 == nullptr || router_logits == nullptr || out_bf16 == nullptr || ws == nullptr)
+        return fail(NVFP4_EINVAL, "moe: null x / logits / out / ws");
+    rc = check_tensor(w1, "moe w1");
+    if (rc) return rc;
+    rc = check_tensor(w2, "moe w2");
+    if (rc) return rc;
+    if (w1->rows != (int64_t)E * 2 * F || w1->cols != H)
+        return fail(NVFP4_EINVAL, "moe: w1 must be [E*2F x H]");
+    if (w2->rows != (int64_t)E * H || w2->cols != F) return fail(NVFP4_EINVAL, "moe: w2 must be [E*H x F]");
+    if (!aligned(x_bf16, 16) || !aligned(router_logits, 16) || !aligned(out_bf16, 16) ||
+        (router_bias != nullptr && !aligned(router_bias, 4)))
+        return fail(NVFP4_EALIGN, "moe: x, logits and out must be 16-byte aligned");
+    if (!aligned(ws, 256)) return fail(NVFP4_EALIGN, "moe: ws must be 256-byte aligned");
+    if (ws_bytes < L.total)
+        return fail(NVFP4_EWORKSPACE, "moe: workspace %zu < required %zu bytes", ws_bytes, L.total);
+    if (dbg != nullptr && dbg->fc1_out != nullptr && !aligned(dbg->fc1_out, 16))
+        return fail(NVFP4_EALIGN, "moe: dbg->fc1_out must be 16-byte aligned");
+    if (sm_count() <= 0) return fail(NVFP4_ELAUNCH, "moe: no CUDA device");
+    const bool at_fc1 = opt != nullptr && opt->weight_at_fc1 != 0;
+    uint8_t* base = reinterpret_cast<uint8_t*>(ws);
+    auto at = [&](size_t off) { return base + off; };
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t R = T * topk;
+    cudaError_t e;
+    void** ev = dbg ? dbg->stage_events : nullptr;
+    int ev_i = 0;
+    auto mark = [&]() -> cudaError_t {
+        if (ev == nullptr) return cudaSuccess;
+        return cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[ev_i++]), s);
+    };
+    if ((e = mark()) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe event: %s", cudaGetErrorString(e));
+
+    // 1. per-token quantization of X (once per token; the permute moves the result)
+    nvfp4::QuantLaunch qx{};
+    qx.x = x_bf16;
+    qx.ld = H;
+    qx.rows = T;
+    qx.cols = H;
+    qx.codes = at(L.xq_codes);
+    qx.sf = at(L.xq_sf);
+    qx.scale = reinterpret_cast<float*>(at(L.xq_scale));
+    if ((e = nvfp4::launch_quantize(qx, s)) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe quantize: %s", cudaGetErrorString(e));
+    if ((e = mark()) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe event: %s", cudaGetErrorString(e));
+
+    // 2. routing, metadata and permute
+    nvfp4::RouteLaunch r{};
+    r.logits = router_logits;
+    r.bias = router_bias;
+    r.T = T;
+    r.E = E;
+    r.k = topk;
+    r.ids = reinterpret_cast<int*>(at(L.ids));
+    r.w = reinterpret_cast<float*>(at(L.weights));
+    const int64_t nchunks = (T + nvfp4::kRouteChunk - 1) / nvfp4::kRouteChunk;
+    r.chunk_cnt = reinterpret_cast<int*>(at(L.chunk_counts));
+    r.chunk_base = r.chunk_cnt + nchunks * E;
+    r.cnt = reinterpret_cast<int*>(at(L.counts));
+    r.off = reinterpret_cast<int*>(at(L.offsets));
+    r.poff = reinterpret_cast<int*>(at(L.padded_offsets));
+    r.done = reinterpret_cast<unsigned int*>(at(L.err) + 4);
+    r.perm = reinterpret_cast<int*>(at(L.perm));
+    r.inv = reinterpret_cast<int*>(at(L.inv));
+    r.err = reinterpret_cast<uint32_t*>(at(L.err));
+    r.xq_codes = at(L.xq_codes);
+    r.xq_sf = at(L.xq_sf);
+    r.xq_scale = reinterpret_cast<const float*>(at(L.xq_scale));
+    r.H = H;
+    r.a1_codes = at(L.a1_codes);
+    r.a1_sf = at(L.a1_sf);
+    r.a1_scale = reinterpret_cast<float*>(at(L.a1_scale));
+    r.amax2 = reinterpret_cast<float*>(at(L.amax2));
+    r.row_w = at_fc1 ? reinterpret_cast<float*>(at(L.row_weights)) : nullptr;
+    if ((e = nvfp4::launch_route(r, s)) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe route: %s", cudaGetErrorString(e));
+    if ((e = mark()) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe event: %s", cudaGetErrorString(e));
+
+    // 3. FC1 grouped GEMM, SwiGLU + row-amax epilogue
+    nvfp4::GemmLaunch g1{};
+    g1.a_codes = at(L.a1_codes);
+    g1.a_sf = at(L.a1_sf);
+    g1.a_scale = reinterpret_cast<const float*>(at(L.a1_scale));
+    g1.M = R;
+    g1.b_codes = w1->codes;
+    g1.b_sf = w1->sf;
+    g1.b_scale = w1->scale;
+    g1.N = (int)(2 * F);
+    g1.K = (int)H;
+    g1.G = E;
+    g1.goff = r.off;
+    g1.gpoff = r.poff;
+    g1.mode = 1;
+    g1.out = at(L.d);
+    g1.ldo = F;
+    g1.amax_out = reinterpret_cast<float*>(at(L.amax2));
+    g1.row_prob = r.row_w;
+    g1.c_debug = dbg ? dbg->fc1_out : nullptr;
+    g1.err = r.err;
+    g1.num_sms = sm_count();
+    if ((e = nvfp4::launch_gemm(g1, s)) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe fc1: %s", cudaGetErrorString(e));
+    if ((e = mark()) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe event: %s", cudaGetErrorString(e));
+
+    // 4. requantize D per row, reusing the epilogue's amax
+    nvfp4::QuantLaunch q2{};
+    q2.x = at(L.d);
+    q2.ld = F;
+    q2.rows = R;
+    q2.cols = F;
+    q2.amax_in = reinterpret_cast<const float*>(at(L.amax2));
+    q2.codes = at(L.a2_codes);
+    q2.sf = at(L.a2_sf);
+    q2.scale = reinterpret_cast<float*>(at(L.a2_scale));
+    q2.goff = r.off;
+    q2.gpoff = r.poff;
+    q2.G = E;
+    if ((e = nvfp4::launch_quantize(q2, s)) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe requant: %s", cudaGetErrorString(e));
+    if ((e = mark()) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe event: %s", cudaGetErrorString(e));
+
+    // 5. FC2 grouped GEMM -> bf16 Y2
+    nvfp4::GemmLaunch g2{};
+    g2.a_codes = at(L.a2_codes);
+    g2.a_sf = at(L.a2_sf);
+    g2.a_scale = reinterpret_cast<const float*>(at(L.a2_scale));
+    g2.M = R;
+    g2.b_codes = w2->codes;
+    g2.b_sf = w2->sf;
+    g2.b_scale = w2->scale;
+    g2.N = (int)H;
+    g2.K = (int)F;
+    g2.G = E;
+    g2.goff = r.off;
+    g2.gpoff = r.poff;
+    g2.mode = 0;
+    g2.out = at(L.y2);
+    g2.ldo = H;
+    g2.err = r.err;
+    g2.num_sms = sm_count();
+    if ((e = nvfp4::launch_gemm(g2, s)) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe fc2: %s", cudaGetErrorString(e));
+    if ((e = mark()) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe event: %s", cudaGetErrorString(e));
+
+    // 6. router-weighted combine
+    nvfp4::CombineLaunch c{};
+    c.y = at(L.y2);
+    c.inv = r.inv;
+    c.w = at_fc1 ? nullptr : r.w;
+    c.T = T;
+    c.H = H;
+    c.k = topk;
+    c.out = out_bf16;
+    if ((e = nvfp4::launch_combine(c, s)) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe combine: %s", cudaGetErrorString(e));
+    if ((e = mark()) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe event: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,95 @@
+// kernels.h -- internal launch interfaces between the C ABI layer (api.cu)
+// and the kernel files.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace nvfp4 {
+
+struct QuantLaunch {
+    const void* x;          // bf16 [rows x cols], row stride ld elements
+    int64_t ld, rows, cols;
+    const float* amax_in;   // nullable
+    int per_tensor;
+    uint8_t* codes;
+    uint8_t* sf;
+    float* scale;
+    const int* goff;        // nullable: scale rows remapped by group padding
+    const int* gpoff;
+    int G;
+    void* ws;               // >= 4 bytes when per_tensor && !amax_in
+};
+cudaError_t launch_quantize(const QuantLaunch& q, cudaStream_t stream);
+
+// Grouped / dense block-scaled NVFP4 GEMM on tcgen05.
+//   A rows [M_total x K] (codes + swizzled scales padded per group by
+//   gpoff + per-row fp32 scale); B per group [N x K] (codes + swizzled
+//   scales + one fp32 scale per group).  Mode 0 writes bf16 [M x N]; mode 1
+//   (SwiGLU) reads B rows [gate F | up F] (N = 2F) and writes bf16 D [M x F]
+//   plus a per-row atomic amax of D.
+struct GemmLaunch {
+    const uint8_t* a_codes;
+    const uint8_t* a_sf;
+    const float* a_scale;
+    int64_t M;             // rows of A (dense) or the bound on rows (grouped)
+    const uint8_t* b_codes;
+    const uint8_t* b_sf;
+    const float* b_scale;  // [G]
+    int N, K, G;
+    const int* goff;       // nullable (dense: one group of M rows)
+    const int* gpoff;
+    int mode;              // 0 plain, 1 SwiGLU
+    void* out;             // bf16
+    int64_t ldo;
+    float* amax_out;       // mode 1
+    const float* row_prob; // mode 1, nullable: D *= row_prob[row] (router weight at FC1)
+    float* c_debug;        // mode 1, nullable: fp32 [M x N] pre-activation
+    uint32_t* err;         // nullable
+    int num_sms;
+};
+cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t stream);
+
+struct RouteLaunch {
+    const float* logits;   // [T x E]
+    const float* bias;     // nullable
+    int64_t T;
+    int E, k;
+    int* ids;              // [T x k]
+    float* w;              // [T x k]
+    int* chunk_cnt;        // [nchunks x E]
+    int* chunk_base;       // [nchunks x E]
+    int* cnt;              // [E]
+    int* off;              // [E+1]
+    int* poff;             // [E+1]
+    unsigned int* done;    // one counter word, zero before the call, left zero after
+    int* perm;             // [T*k]
+    int* inv;              // [T*k]
+    uint32_t* err;
+    // permute (gather quantized X rows into expert order)
+    const uint8_t* xq_codes;
+    const uint8_t* xq_sf;
+    const float* xq_scale;
+    int64_t H;
+    uint8_t* a1_codes;
+    uint8_t* a1_sf;
+    float* a1_scale;
+    float* amax2;          // zeroed here for the FC1 epilogue ([T*k])
+    float* row_w;          // nullable: [T*k] router weight of each expert-ordered row
+};
+constexpr int kRouteChunk = 128;  // tokens per chunk of the stable scatter
+cudaError_t launch_route(const RouteLaunch& r, cudaStream_t stream);
+
+struct CombineLaunch {
+    const void* y;         // bf16 [R x H]
+    const int* inv;        // [T x k]
+    const float* w;        // [T x k], nullable = weights of 1
+    int64_t T, H;
+    int k;
+    void* out;             // bf16 [T x H]
+};
+cudaError_t launch_combine(const CombineLaunch& c, cudaStream_t stream);
+
+int device_sm_count();
+
+}  // namespace nvfp4

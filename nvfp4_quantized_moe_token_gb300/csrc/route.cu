@@ -1,0 +1,229 @@
+// route.cu -- router top-k, device-side routing metadata, and the permute of
+// the per-token quantized rows into expert order (sm_103a).
+//
+// "miniTE Technical Report" 5.2: expert boundaries are offsets built on the
+// device (no host-to-device metadata copies, no host sync), zero-token
+// experts and padding handled in the same grouped path; 5.3: the quantized
+// activation travels with its scales through the reorder.  Routing: top-8 of
+// 128 experts ("miniTE Technical Report" 6.4 D15 profiles).
+//
+// Three kernels, all deterministic:
+//   1. route_topk: one warp per token -- z = logit + bias, k rounds of warp
+//      argmax (ties to the lower expert), softmax over the k selected z;
+//      per-chunk expert histogram in shared memory.
+//   2. route_scan: one block per expert scans its chunk counts; the last
+//      block to finish turns the expert totals into offsets and padded
+//      offsets.
+//   3. route_scatter: one block per chunk ranks each (token, slot) inside its
+//      expert by a shared-memory bitmap (stable: ascending token index),
+//      writes perm / inv, and copies the token's codes, scales and outer
+//      scale to every expert row it was routed to.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace nvfp4 {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+template <int EPL>  // experts per lane: E = 32 * EPL
+__global__ void __launch_bounds__(kThreads) route_topk_kernel(RouteLaunch p) {
+    __shared__ int scnt[32 * EPL];
+    const int E = 32 * EPL;
+    for (int e = threadIdx.x; e < E; e += kThreads) scnt[e] = 0;
+    if (blockIdx.x == 0 && threadIdx.x == 0) *p.done = 0u;
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t t0 = (int64_t)blockIdx.x * kRouteChunk;
+    for (int i = warp; i < kRouteChunk; i += kWarps) {
+        const int64_t t = t0 + i;
+        if (t >= p.T) break;
+        float z[EPL];
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) {
+            const int e = lane + 32 * j;
+            const float b = p.bias ? __ldg(p.bias + e) : 0.0f;
+            z[j] = __fadd_rn(__ldg(p.logits + t * E + e), b);
+        }
+        uint32_t taken = 0;
+        float my_z = 0.0f;
+        int my_id = 0;
+        for (int s = 0; s < p.k; ++s) {
+            float bv = -INFINITY;
+            int bi = 0x7fffffff;
+#pragma unroll
+            for (int j = 0; j < EPL; ++j)
+                if (!((taken >> j) & 1u) && z[j] > bv) { bv = z[j]; bi = lane + 32 * j; }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+            }
+            if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+            if (lane == s) { my_z = bv; my_id = bi; }
+        }
+        // weights: softmax over the selected z, summed in slot order
+        const float zmax = __shfl_sync(0xffffffffu, my_z, 0);
+        const float ex = lane < p.k ? expf(__fsub_rn(my_z, zmax)) : 0.0f;
+        float sum = 0.0f;
+        for (int s = 0; s < p.k; ++s) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, ex, s));
+        if (lane < p.k) {
+            p.ids[t * p.k + lane] = my_id;
+            p.w[t * p.k + lane] = __fdiv_rn(ex, sum);
+            atomicAdd(&scnt[my_id], 1);
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kThreads) p.chunk_cnt[(int64_t)blockIdx.x * E + e] = scnt[e];
+}
+
+// Block-wide exclusive scan of one int per thread (kThreads threads).
+__device__ __forceinline__ int block_exclusive_scan(int v, int* total) {
+    __shared__ int warp_sums[kWarps];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    int before = 0, all = 0;
+    for (int w = 0; w < kWarps; ++w) {
+        if (w < warp) before += warp_sums[w];
+        all += warp_sums[w];
+    }
+    __syncthreads();
+    *total = all;
+    return before + incl - v;
+}
+
+__global__ void __launch_bounds__(kThreads) route_scan_kernel(RouteLaunch p, int nchunks) {
+    const int E = p.E;
+    const int e = blockIdx.x;
+    const int per = (nchunks + kThreads - 1) / kThreads;
+    const int c0 = threadIdx.x * per;
+    int local = 0;
+    for (int c = c0; c < c0 + per && c < nchunks; ++c) local += p.chunk_cnt[(int64_t)c * E + e];
+    int total;
+    int base = block_exclusive_scan(local, &total);
+    for (int c = c0; c < c0 + per && c < nchunks; ++c) {
+        p.chunk_base[(int64_t)c * E + e] = base;
+        base += p.chunk_cnt[(int64_t)c * E + e];
+    }
+    __shared__ int is_last;
+    if (threadIdx.x == 0) {
+        p.cnt[e] = total;
+        __threadfence();
+        is_last = atomicAdd(p.done, 1u) == (unsigned)(E - 1);
+    }
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    // the last expert block: offsets and 128-padded offsets over all experts
+    const int c = threadIdx.x < E ? __ldcg(p.cnt + threadIdx.x) : 0;
+    int tot1, tot2;
+    const int o1 = block_exclusive_scan(c, &tot1);
+    const int o2 = block_exclusive_scan((c + 127) / 128 * 128, &tot2);
+    if (threadIdx.x < E) { p.off[threadIdx.x] = o1; p.poff[threadIdx.x] = o2; }
+    if (threadIdx.x == 0) { p.off[E] = tot1; p.poff[E] = tot2; }
+}
+
+__global__ void __launch_bounds__(kThreads) route_scatter_kernel(RouteLaunch p) {
+    extern __shared__ int smem[];
+    const int E = p.E, k = p.k;
+    const int nslot = kRouteChunk * k;
+    uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem);   // [E][kRouteChunk/32]
+    int* sid = smem + E * (kRouteChunk / 32);                // [nslot] expert ids
+    int* spos = sid + nslot;                                 // [nslot] expert-ordered row
+    int* sprow = spos + nslot;                               // [nslot] padded scale row
+    const int64_t t0 = (int64_t)blockIdx.x * kRouteChunk;
+    for (int i = threadIdx.x; i < E * (kRouteChunk / 32); i += kThreads) bitmap[i] = 0u;
+    __syncthreads();
+    for (int i = threadIdx.x; i < nslot; i += kThreads) {
+        const int tl = i / k;
+        const int64_t t = t0 + tl;
+        int e = -1;
+        if (t < p.T) {
+            e = p.ids[t0 * k + i];
+            if (e < 0 || e >= E) { atomicOr(p.err, NVFP4_DEVERR_BADEXPERT); e = -1; }
+            else atomicOr(&bitmap[e * (kRouteChunk / 32) + (tl >> 5)], 1u << (tl & 31));
+        }
+        sid[i] = e;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < nslot; i += kThreads) {
+        const int e = sid[i];
+        if (e < 0) continue;
+        const int tl = i / k;
+        const uint32_t* bm = bitmap + e * (kRouteChunk / 32);
+        int rank = __popc(bm[tl >> 5] & ((1u << (tl & 31)) - 1u));
+        for (int w = 0; w < (tl >> 5); ++w) rank += __popc(bm[w]);
+        const int off = __ldg(p.off + e);
+        const int pos = off + p.chunk_base[(int64_t)blockIdx.x * E + e] + rank;
+        const int64_t ts = t0 * k + i;  // = t * k + slot
+        p.perm[pos] = (int)ts;
+        p.inv[ts] = pos;
+        p.amax2[pos] = 0.0f;
+        if (p.row_w) p.row_w[pos] = p.w[ts];
+        spos[i] = pos;
+        sprow[i] = __ldg(p.poff + e) + (pos - off);
+    }
+    __syncthreads();
+    // copy each token's quantized row to its k expert rows
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t row_bytes = p.H / 2;
+    const int64_t sp4 = p.H / 64;  // scale-column groups per row
+    for (int tl = warp; tl < kRouteChunk; tl += kWarps) {
+        const int64_t t = t0 + tl;
+        if (t >= p.T) break;
+        const uint8_t* src = p.xq_codes + t * row_bytes;
+        for (int64_t c = lane * 16; c < row_bytes; c += 512) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + c));
+            for (int s = 0; s < k; ++s) {
+                const int pos = spos[tl * k + s];
+                if (pos >= 0 && sid[tl * k + s] >= 0)
+                    *reinterpret_cast<uint4*>(p.a1_codes + (int64_t)pos * row_bytes + c) = v;
+            }
+        }
+        for (int64_t q = lane; q < sp4; q += 32) {
+            const uint32_t g = __ldg(reinterpret_cast<const uint32_t*>(p.xq_sf + sf_group_offset(t, q, sp4)));
+            for (int s = 0; s < k; ++s) {
+                if (sid[tl * k + s] < 0) continue;
+                *reinterpret_cast<uint32_t*>(p.a1_sf + sf_group_offset(sprow[tl * k + s], q, sp4)) = g;
+            }
+        }
+        if (lane < k && sid[tl * k + lane] >= 0) p.a1_scale[spos[tl * k + lane]] = __ldg(p.xq_scale + t);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_route(const RouteLaunch& r, cudaStream_t stream) {
+    const int nchunks = (int)((r.T + kRouteChunk - 1) / kRouteChunk);
+    switch (r.E / 32) {
+        case 1: route_topk_kernel<1><<<nchunks, kThreads, 0, stream>>>(r); break;
+        case 2: route_topk_kernel<2><<<nchunks, kThreads, 0, stream>>>(r); break;
+        case 3: route_topk_kernel<3><<<nchunks, kThreads, 0, stream>>>(r); break;
+        case 4: route_topk_kernel<4><<<nchunks, kThreads, 0, stream>>>(r); break;
+        case 5: route_topk_kernel<5><<<nchunks, kThreads, 0, stream>>>(r); break;
+        case 6: route_topk_kernel<6><<<nchunks, kThreads, 0, stream>>>(r); break;
+        case 7: route_topk_kernel<7><<<nchunks, kThreads, 0, stream>>>(r); break;
+        case 8: route_topk_kernel<8><<<nchunks, kThreads, 0, stream>>>(r); break;
+        default: return cudaErrorInvalidValue;  // E is validated by the caller
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    route_scan_kernel<<<r.E, kThreads, 0, stream>>>(r, nchunks);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const size_t smem = sizeof(int) * ((size_t)r.E * (kRouteChunk / 32) + 3 * (size_t)kRouteChunk * r.k);
+    route_scatter_kernel<<<nchunks, kThreads, smem, stream>>>(r);
+    return cudaGetLastError();
+}
+
+}  // namespace nvfp4

@@ -277,13 +277,15 @@ def combine(y, inv, w):
     return out
 
 
-def moe_forward(x_bf16, logits, bias, w1q, w2q, k, rows=None):
+def moe_forward(x_bf16, logits, bias, w1q, w2q, k, rows=None, w_deq=None):
     """Whole expert layer on the CPU, each stage from the previous oracle stage.
 
     w1q / w2q: lists over experts of (codes, sf_lin, scale[1]) per-tensor
     quantized weights, W1_e [2F, H] = gate | up, W2_e [H, F].
     rows (nullable): restrict the output to these token indices (the router,
     metadata and every expert GEMM row needed by them are still computed).
+    w_deq (nullable): (list of dequantize(w1q[e]), list of dequantize(w2q[e]))
+    computed once for static weights.
     Returns a dict of every intermediate."""
     E = len(w1q)
     ids, w = route(logits, bias, k)
@@ -306,13 +308,15 @@ def moe_forward(x_bf16, logits, bias, w1q, w2q, k, rows=None):
         sel = np.nonzero(need[lo:hi])[0] + lo
         if len(sel) == 0:
             continue
+        b1 = w_deq[0][e] if w_deq is not None else dequantize(*w1q[e], per_tensor=True)
+        b2 = w_deq[1][e] if w_deq is not None else dequantize(*w2q[e], per_tensor=True)
         a = dequantize(a1[0][sel], a1[1][sel], a1[2][sel])
-        c = gemm_f64(a, dequantize(*w1q[e], per_tensor=True))
+        c = gemm_f64(a, b1)
         d, am = swiglu(c)
         d_all[sel] = d
         amax2[sel] = am
         q2 = quantize(d, amax_in=am)
-        y2[sel] = bf16_to_f64(bf16_round(gemm_f64(dequantize(*q2), dequantize(*w2q[e], per_tensor=True))))
+        y2[sel] = bf16_to_f64(bf16_round(gemm_f64(dequantize(*q2), b2)))
     if rows is None:
         out = combine(y2, meta["inv"], w)
     else:

@@ -242,13 +242,17 @@ void orc_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
 void orc_dequantize(const uint8_t* codes, const uint8_t* sf_lin, const float* scale,
                     int64_t rows, int64_t cols, int per_tensor, double* out) {
     const int64_t nblk = cols / 16;
+    e4m3_table_init();
     for (int64_t r = 0; r < rows; ++r) {
         double sg = per_tensor ? (double)scale[0] : (double)scale[r];
-        for (int64_t j = 0; j < cols; ++j) {
-            uint8_t byte = codes[r * (cols / 2) + j / 2];
-            uint8_t c = (j & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
-            double sb = orc_e4m3_decode(sf_lin[r * nblk + j / 16]);
-            out[r * cols + j] = orc_e2m1_decode(c) * sb * sg;
+        for (int64_t b = 0; b < nblk; ++b) {
+            uint8_t s = sf_lin[r * nblk + b];
+            double sb = s < 127 ? E4M3_POS[s] : orc_e4m3_decode(s);
+            for (int64_t j = b * 16; j < b * 16 + 16; ++j) {
+                uint8_t byte = codes[r * (cols / 2) + j / 2];
+                uint8_t c = (j & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
+                out[r * cols + j] = orc_e2m1_decode(c) * sb * sg;
+            }
         }
     }
 }

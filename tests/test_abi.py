@@ -1,0 +1,107 @@
+"""The C-ABI library builds, loads without a GPU, exports every symbol that
+include/nvfp4moe.h declares, and rejects bad arguments on the host before
+any launch (CPU only: no compute call reaches the device)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import nvfp4_quantized_moe_token_gb300 as nv
+from nvfp4_quantized_moe_token_gb300 import build as nvbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nvfp4moe.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    nvbuild.build()
+    return nv.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return re.findall(r"NVFP4_API\s+[\w\s\*]+?\b(\w+)\s*\(", src)
+
+
+def test_header_declares_the_binding_symbols():
+    assert sorted(declared_functions()) == sorted(nv.SYMBOLS)
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+    out = os.popen(f"nm -D --defined-only {nv.library_path()}").read().split()
+    exported = {w for w in out if not w.startswith("_") and w.islower()}
+    assert set(declared_functions()) <= exported
+
+
+def test_sizing_functions(L):
+    assert nv.sf_bytes(16384, 2048) == 16384 * 128
+    assert nv.sf_bytes(1, 16) == 128 * 4
+    assert nv.sf_bytes(130, 768) == 256 * 48
+    assert L.nvfp4_quantize_workspace(10, 64, 0) == 0
+    assert L.nvfp4_quantize_workspace(10, 64, 1) == 256
+    lay = nv.moe_workspace_layout(32768, 2048, 768, 128, 8)
+    R = 32768 * 8
+    assert lay["y2"] + 2 * R * 2048 <= lay["total"]
+    offs = sorted(v for k, v in lay.items() if k != "total")
+    assert all(o % 256 == 0 for o in offs) and len(set(offs)) == len(offs)
+    assert L.moe_expert_workspace(32768, 2048, 768, 128, 8) == lay["total"]
+
+
+def _t(rows, cols, ptr=4096):
+    return nv._Tensor(ptr, ptr, ptr, rows, cols)
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(x=None), -1),
+    (dict(cols=24), -2),
+    (dict(mode=7), -1),
+    (dict(ld=8), -1),
+    (dict(x=4100), -3),
+    (dict(mode=1, ws=None), -4),
+])
+def test_quantize_rejects_bad_arguments(L, args, code):
+    a = dict(x=4096, rows=4, cols=32, ld=32, mode=0, ws=None)
+    a.update(args)
+    out = _t(a["rows"], a["cols"])
+    rc = L.nvfp4_quantize_rows(a["x"], a["rows"], a["cols"], a["ld"], a["mode"], None, ctypes.byref(out),
+                               a["ws"], 0, None)
+    assert rc == code
+    assert L.nvfp4_last_error().decode()
+
+
+def test_linear_rejects_bad_shapes(L):
+    x, w = _t(64, 96), _t(512, 96)
+    assert L.nvfp4_linear(ctypes.byref(x), ctypes.byref(w), 4096, 512, None, 0, None) == -2
+    x, w = _t(64, 256), _t(500, 256)
+    assert L.nvfp4_linear(ctypes.byref(x), ctypes.byref(w), 4096, 512, None, 0, None) == -2
+    x, w = _t(64, 256), _t(512, 128)
+    assert L.nvfp4_linear(ctypes.byref(x), ctypes.byref(w), 4096, 512, None, 0, None) == -1
+    x, w = _t(64, 256), _t(512, 256)
+    assert L.nvfp4_linear(ctypes.byref(x), ctypes.byref(w), 4096, 500, None, 0, None) == -3
+
+
+def test_moe_rejects_bad_arguments(L):
+    T, H, F, E, k = 64, 2048, 768, 128, 8
+    w1, w2 = _t(E * 2 * F, H), _t(E * H, F)
+    opt = nv._Options(0)
+    need = L.moe_expert_workspace(T, H, F, E, k)
+
+    def call(**kw):
+        a = dict(x=4096, T=T, H=H, logits=4096, E=E, k=k, w1=w1, w2=w2, F=F, out=4096, ws=4096, wsb=need)
+        a.update(kw)
+        return L.moe_expert_forward(a["x"], a["T"], a["H"], a["logits"], None, a["E"], a["k"],
+                                    ctypes.byref(a["w1"]), ctypes.byref(a["w2"]), a["F"], ctypes.byref(opt),
+                                    a["out"], None, a["ws"], a["wsb"], None)
+    assert call(wsb=need - 1) == -4
+    assert call(H=2000) == -2
+    assert call(E=100) == -2
+    assert call(k=17) == -2
+    assert call(w2=_t(E * H, 2 * F)) == -1
+    assert call(ws=4096 + 16) == -3
+    assert call(x=None) == -1
+    assert call(T=0) == -1

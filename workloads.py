@@ -11,6 +11,9 @@ there are no real activations, weights or DAPO text here, so Gaussian draws
 stand in for them.  Each tensor has its own child stream of the config's
 seed (numpy SeedSequence.spawn), so adding a tensor never shifts another.
 """
+import concurrent.futures as cf
+import os
+
 import numpy as np
 import torch
 
@@ -31,18 +34,48 @@ def bf16_bits_to_f32(h):
 
 
 def _streams(seed, n):
-    return [np.random.default_rng(s) for s in np.random.SeedSequence(seed).spawn(n)]
+    """n independent child seed sequences of `seed` (one per tensor)."""
+    return list(np.random.SeedSequence(seed).spawn(n))
 
 
-def gaussian_bf16(rng, shape, std=1.0, outlier_frac=0.0, outlier_mult=50.0, zero_row_frac=0.0):
+def _draw(rng, shape, std, outlier_frac, outlier_mult, zero_row_frac):
     x = rng.standard_normal(shape, dtype=np.float32)
     if std != 1.0:
         x *= np.float32(std)
     if outlier_frac > 0:
         x[rng.random(shape) < outlier_frac] *= np.float32(outlier_mult)
     if zero_row_frac > 0:
-        x[rng.random(shape[0]) < zero_row_frac] = 0.0
+        rows = x.reshape(-1, shape[-1])
+        rows[rng.random(rows.shape[0]) < zero_row_frac] = 0.0
     return to_bf16_bits(x)
+
+
+def gaussian_bf16(src, shape, std=1.0, outlier_frac=0.0, outlier_mult=50.0, zero_row_frac=0.0):
+    """bf16 bit patterns of N(0, std^2) draws; a fraction of entries scaled by
+    outlier_mult and a fraction of rows (last axis) set to zero.
+
+    src is a numpy Generator (drawn in one piece) or a SeedSequence: then the
+    leading axis is cut into chunks of about 4M elements, each drawn from its
+    own child sequence in a thread pool (numpy releases the GIL while
+    filling), so the values do not depend on the thread count."""
+    if isinstance(src, np.random.Generator):
+        return _draw(src, shape, std, outlier_frac, outlier_mult, zero_row_frac)
+    shape = tuple(shape)
+    per_lead = int(np.prod(shape[1:])) if len(shape) > 1 else 1
+    step = max(1, (1 << 22) // per_lead)
+    starts = list(range(0, shape[0], step))
+    seqs = src.spawn(len(starts))
+    out = np.empty(shape, np.uint16)
+
+    def one(i):
+        lo = starts[i]
+        hi = min(shape[0], lo + step)
+        out[lo:hi] = _draw(np.random.default_rng(seqs[i]), (hi - lo,) + shape[1:], std,
+                           outlier_frac, outlier_mult, zero_row_frac)
+
+    with cf.ThreadPoolExecutor(min(16, os.cpu_count() or 1)) as ex:
+        list(ex.map(one, range(len(starts))))
+    return out
 
 
 def linear_small(seed=0):
@@ -50,7 +83,7 @@ def linear_small(seed=0):
     ~N(0, 0.02^2) and handed to the GEMM K-major as [512 x 256]."""
     rx, rw = _streams(seed, 2)
     x = gaussian_bf16(rx, (64, 256))
-    w_kn = rw.standard_normal((256, 512), dtype=np.float32) * np.float32(0.02)
+    w_kn = np.random.default_rng(rw).standard_normal((256, 512), dtype=np.float32) * np.float32(0.02)
     w = to_bf16_bits(np.ascontiguousarray(w_kn.T))
     return dict(x=x, w=w)
 
@@ -69,8 +102,8 @@ def moe_layer(seed, tokens, bias_std, hidden=HIDDEN, experts=EXPERTS, ffn=FFN,
     rx, rl, rb, r1, r2 = _streams(seed, 5)
     out = dict(
         x=gaussian_bf16(rx, (tokens, hidden)),
-        logits=rl.standard_normal((tokens, experts), dtype=np.float32),
-        bias=(rb.standard_normal(experts, dtype=np.float32) * np.float32(bias_std)),
+        logits=np.random.default_rng(rl).standard_normal((tokens, experts), dtype=np.float32),
+        bias=(np.random.default_rng(rb).standard_normal(experts, dtype=np.float32) * np.float32(bias_std)),
     )
     if with_weights:
         out["w1"] = gaussian_bf16(r1, (experts, 2 * ffn, hidden), std=0.02)
