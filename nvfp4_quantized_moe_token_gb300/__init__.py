@@ -205,6 +205,10 @@ def moe_expert_forward(x, logits, bias, w1q, w2q, F, topk, weight_at_fc1=False, 
     evs = None
     if stage_events is not None:
         assert len(stage_events) == len(STAGES) + 1
+        st = stream if stream is not None else torch.cuda.current_stream()
+        for e in stage_events:
+            if e.cuda_event == 0:  # torch creates the CUDA event on its first record
+                e.record(st)
         evs = (c_vp * len(stage_events))(*[e.cuda_event for e in stage_events])
     dbg = _Debug(None if fc1_debug is None else fc1_debug.data_ptr(), evs)
     rc = lib().moe_expert_forward(_ptr(x), T, H, _ptr(logits), _ptr(bias), E, topk, ctypes.byref(a),

@@ -1,9 +1,10 @@
 // combine.cu -- router-weighted unpermute that ends the expert layer (sm_103a).
 //
 // out[t] = bf16( sum_{slot=0..k-1} w[t, slot] * Y2[inv[t, slot]] ), fp32
-// accumulation in slot order (deterministic).  One warp per token; a lane
-// owns 8 consecutive columns per 256-column step, so every Y2 row read and
-// the output row write are 16-byte coalesced.
+// accumulation in slot order (deterministic).  One block per token; a thread
+// owns 8 consecutive columns per 2048-column step and has the k row loads of
+// a step in flight together; every Y2 row read and the output row write are
+// 16-byte coalesced.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -14,9 +15,7 @@ namespace {
 constexpr int kThreads = 256;
 
 __global__ void __launch_bounds__(kThreads) combine_kernel(CombineLaunch c) {
-    const int lane = threadIdx.x & 31;
-    const int64_t t = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
-    if (t >= c.T) return;
+    const int64_t t = blockIdx.x;
     const __nv_bfloat16* y = reinterpret_cast<const __nv_bfloat16*>(c.y);
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(c.out) + t * c.H;
     int row[16];
@@ -28,13 +27,16 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(CombineLaunch c) {
             w[s] = c.w ? __ldg(c.w + t * c.k + s) : 1.0f;
         }
     }
-    for (int64_t col = lane * 8; col < c.H; col += 256) {
+    for (int64_t col = threadIdx.x * 8; col < c.H; col += kThreads * 8) {
+        uint4 v[16];
+#pragma unroll
+        for (int s = 0; s < 16; ++s)  // all k row loads in flight before any use
+            if (s < c.k) v[s] = __ldg(reinterpret_cast<const uint4*>(y + (int64_t)row[s] * c.H + col));
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
         for (int s = 0; s < 16; ++s) {
             if (s < c.k) {
-                const uint4 v = __ldg(reinterpret_cast<const uint4*>(y + (int64_t)row[s] * c.H + col));
-                const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+                const uint32_t wv[4] = {v[s].x, v[s].y, v[s].z, v[s].w};
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     acc[2 * j] = fmaf(w[s], __uint_as_float(wv[j] << 16), acc[2 * j]);
@@ -56,8 +58,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(CombineLaunch c) {
 
 cudaError_t launch_combine(const CombineLaunch& c, cudaStream_t stream) {
     if (c.T == 0) return cudaSuccess;
-    const int warps = kThreads / 32;
-    combine_kernel<<<(unsigned)((c.T + warps - 1) / warps), kThreads, 0, stream>>>(c);
+    combine_kernel<<<(unsigned)c.T, kThreads, 0, stream>>>(c);
     return cudaGetLastError();
 }
 

@@ -7,19 +7,25 @@
 // x alpha_b; C = gate | up; D = act(gate, up) (x prob); amax of D reduced
 // concurrently across CTAs).
 //
-// Persistent kernel, one CTA per SM, warp-specialized:
-//   warp 0      TMA producer: A tile 128 x 256 FP4 (128B-swizzled), B tile
-//               256 x 256 FP4 (two 128-row boxes), and the tiles' E4M3 scale
-//               atoms (plain bulk copies: the quantizer already wrote them in
-//               the MMA's layout) into a 4-stage shared-memory ring.
-//   warp 1      TMEM allocator and MMA issuer: per stage, tcgen05.cp of the
-//               scale atoms into TMEM, then four
-//               tcgen05.mma.kind::mxf4nvf4.block_scale (M=128, N=256, K=64)
-//               accumulating fp32 in TMEM; tcgen05.commit frees the stage.
-//   warps 2-9   epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
-//               lane quarter w%4, column half (w-2)/4), alpha scaling, then
-//               either bf16 out (mode 0) or SwiGLU -> bf16 D + row amax
-//               (mode 1).
+// Persistent kernel, one CTA per SM, 22 warps with fixed roles:
+//   warp 0       TMA producer: per K-stage the A tile (128 rows x 256 FP4,
+//                128B-swizzled), the B tile (256 rows: two 128-row boxes) and
+//                the E4M3 scale atoms of both (plain bulk copies: the
+//                quantizer wrote them in the MMA's layout), 4-stage ring.
+//   warp 1       TMEM allocator and MMA issuer: per stage four
+//                tcgen05.mma.kind::mxf4nvf4.block_scale (M=128, N=256,
+//                K=64), fp32 accumulation in TMEM; tcgen05.commit frees the
+//                smem stage and, after the last stage, hands the accumulator
+//                to the epilogue.
+//   warps 2-5    scale writers (one per TMEM lane quarter): move each stage's
+//                scale atoms from shared memory into TMEM with tcgen05.st.
+//                (tcgen05.cp would do the same copy, but every cp instruction
+//                occupies the tensor pipe for ~55-80 cycles whatever its size,
+//                three of them per MMA; tcgen05.st runs on the warps.)
+//   warps 6-21   epilogue: each warp copies its 32 rows x 64 accumulator
+//                columns into registers, releases TMEM at once (the next
+//                tile's MMAs start), then scales and either stores bf16
+//                (mode 0) or computes SwiGLU -> bf16 D + row amax (mode 1).
 // Tiles are ordered (padded m-tile, n-tile) with n fastest, so CTAs running
 // at the same time share the A rows and one expert's weights in L2.
 // Every pipeline wait is bounded in time; a wait that runs out raises an
@@ -45,8 +51,9 @@ constexpr int B_BYTES = BN * BK / 2;    // 32 KB
 constexpr int ATOMS = BK / 64;          // scale atoms (128 rows x 4 scales) per 128 rows per stage
 constexpr int SFA_BYTES = ATOMS * 512;  // 2 KB
 constexpr int SFB_BYTES = 2 * ATOMS * 512;
-constexpr int EPI_WARPS = 8;
-constexpr int THREADS = 64 + EPI_WARPS * 32;
+constexpr int EPI_WARP0 = 6;            // warps 6..21 run the epilogue (2..5 write scales)
+constexpr int EPI_WARPS = 16;
+constexpr int THREADS = (EPI_WARP0 + EPI_WARPS) * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;
 constexpr uint32_t SF_COL = 256;        // per stage: SFA 4 atoms x 4 cols, SFB 8 atoms x 4 cols
@@ -59,14 +66,15 @@ struct __align__(1024) Smem {
     uint8_t b[STAGES][B_BYTES];
     uint8_t sfa[STAGES][SFA_BYTES];
     uint8_t sfb[STAGES][SFB_BYTES];
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
+    uint64_t full[STAGES];      // TMA bytes landed
+    uint64_t sf_full[STAGES];   // scales of the stage written to TMEM (4 warps)
+    uint64_t empty[STAGES];     // MMAs of the stage done (commit)
     uint64_t tmem_full;
     uint64_t tmem_empty;
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
-    int consumed;           // stages the MMA issuer has taken from the ring
+    int consumed;               // stages the MMA issuer has taken from the ring
     int goff[MAX_G + 1];
     int gpoff[MAX_G + 1];
 };
@@ -110,26 +118,16 @@ __device__ __forceinline__ Tile decode_tile(const Smem& s, int G, int n_tiles, i
     return x;
 }
 
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&y)[32]) {
-    uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint32_t w[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            __nv_bfloat162 h = __floats2bfloat162_rn(y[q * 8 + 2 * j], y[q * 8 + 2 * j + 1]);
-            w[j] = *reinterpret_cast<uint32_t*>(&h);
-        }
-        d4[q] = make_uint4(w[0], w[1], w[2], w[3]);
-    }
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// silu(g) * u with a sigmoid that cannot overflow: e = exp(-|g|) in (0, 1].
-__device__ __forceinline__ float swiglu1(float g, float u) {
-    const float e = __expf(-fabsf(g));
-    const float r = __frcp_rn(1.0f + e);
-    const float sig = g >= 0.0f ? r : e * r;
-    return g * sig * u;
+// silu(g) = g / (1 + exp(-g)) with the hardware exp2 and reciprocal
+// approximations (a few fp32 ulps, far inside the bf16 rounding that follows);
+// exp(-g) = inf for very negative g gives rcp = 0 and silu = -0, no NaN.
+__device__ __forceinline__ float silu(float g) {
+    return g * rcp_approx(1.0f + __expf(-g));
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -150,7 +148,11 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         for (int i = threadIdx.x; i <= G; i += THREADS) { s.goff[i] = p.goff[i]; s.gpoff[i] = p.gpoff[i]; }
     }
     if (threadIdx.x == 0) {
-        for (int i = 0; i < STAGES; ++i) { mbar_init(smem_u32(&s.full[i]), 1); mbar_init(smem_u32(&s.empty[i]), 1); }
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(smem_u32(&s.full[i]), 1);
+            mbar_init(smem_u32(&s.sf_full[i]), 4);
+            mbar_init(smem_u32(&s.empty[i]), 1);
+        }
         mbar_init(smem_u32(&s.tmem_full), 1);
         mbar_init(smem_u32(&s.tmem_empty), EPI_WARPS);
         mbar_init(smem_u32(&s.drain), 1);
@@ -221,17 +223,12 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 if (!mbar_wait_bounded(smem_u32(&s.tmem_empty), acc_phase ^ 1, abort, p.err)) { ok = false; break; }
                 tc_fence_after();
                 for (int ks = 0; ks < k_stages; ++ks) {
-                    if (!mbar_wait_bounded(smem_u32(&s.full[stage]), phase, abort, p.err)) { ok = false; break; }
+                    if (!mbar_wait_bounded(smem_u32(&s.full[stage]), phase, abort, p.err) ||
+                        !mbar_wait_bounded(smem_u32(&s.sf_full[stage]), phase, abort, p.err)) { ok = false; break; }
                     *(volatile int*)&s.consumed += 1;
                     tc_fence_after();
                     const int na = k_atoms - ks * ATOMS < ATOMS ? k_atoms - ks * ATOMS : ATOMS;
                     const uint32_t sfc = tmem + SF_COL + stage * SF_STAGE_COLS;
-                    const uint32_t sfa0 = smem_u32(s.sfa[stage]), sfb0 = smem_u32(s.sfb[stage]);
-                    for (int kk = 0; kk < na; ++kk) {
-                        tc_cp_sf_atom(sfc + kk * 4, smem_desc(sfa0 + kk * 512, 0, 128, 0));
-                        tc_cp_sf_atom(sfc + 16 + kk * 8, smem_desc(sfb0 + kk * 512, 0, 128, 0));
-                        tc_cp_sf_atom(sfc + 16 + kk * 8 + 4, smem_desc(sfb0 + SFB_BYTES / 2 + kk * 512, 0, 128, 0));
-                    }
                     const uint32_t a0 = smem_u32(s.a[stage]), b0 = smem_u32(s.b[stage]);
                     for (int kk = 0; kk < na; ++kk) {
                         tc_mma_nvfp4(tmem + ACC_COL, smem_desc(a0 + kk * 32, 0, 1024, 2),
@@ -249,78 +246,116 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             tc_commit(smem_u32(&s.drain));
             mbar_wait_drain(smem_u32(&s.drain), 0);
         }
+    } else if (warp < EPI_WARP0) {
+        // ---------------------------------------------------------------- scale writers
+        // Warp w writes TMEM lane quarter w % 4.  Each scale atom (32 lines
+        // of 16 bytes; line i holds the 4 scales of rows i, i+32, i+64, i+96)
+        // goes to 4 consecutive columns of every quarter: thread i of each
+        // quarter writes line i.  SFA atom kk -> columns sfc + 4kk; SFB atom kk
+        // of half hh -> columns sfc + 16 + 8kk + 4hh.
+        const int q = warp & 3;
+        const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            for (int ks = 0; ks < k_stages; ++ks) {
+                if (!mbar_wait_bounded(smem_u32(&s.full[stage]), phase, abort, p.err)) { ok = false; break; }
+                const uint32_t sfc = lane_addr + SF_COL + stage * SF_STAGE_COLS;
+#pragma unroll
+                for (int kk = 0; kk < ATOMS; ++kk) {
+                    const uint4 a = *reinterpret_cast<const uint4*>(s.sfa[stage] + kk * 512 + lane * 16);
+                    const uint4 b0 = *reinterpret_cast<const uint4*>(s.sfb[stage] + kk * 512 + lane * 16);
+                    const uint4 b1 = *reinterpret_cast<const uint4*>(s.sfb[stage] + SFB_BYTES / 2 + kk * 512 + lane * 16);
+                    tmem_st4(sfc + kk * 4, a.x, a.y, a.z, a.w);
+                    tmem_st4(sfc + 16 + kk * 8, b0.x, b0.y, b0.z, b0.w);
+                    tmem_st4(sfc + 20 + kk * 8, b1.x, b1.y, b1.z, b1.w);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&s.sf_full[stage]));
+                if (++stage == STAGES) { stage = 0; phase ^= 1; }
+            }
+        }
     } else {
         // ---------------------------------------------------------------- epilogue
-        const int q = warp & 3;          // TMEM lane quarter this warp may access
-        const int h = (warp - 2) >> 2;   // column half
+        // Each warp copies its 32 rows x 64 accumulator columns into registers
+        // and releases TMEM at once, so the next tile's MMAs run while this
+        // warp scales, activates and stores.
+        const int q = warp & 3;                    // TMEM lane quarter this warp may access
+        const int cg = (warp - EPI_WARP0) >> 2;    // column group 0..3
         const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
             const Tile x = decode_tile(s, G, n_tiles, t);
-            if (!mbar_wait_bounded(smem_u32(&s.tmem_full), acc_phase, abort, p.err)) break;
-            tc_fence_after();
             const int rl = q * 32 + lane;
             const bool valid = rl < x.rows;
             const int64_t row = (int64_t)x.row0 + rl;
-            const float scale = valid ? __fmul_rn(__ldg(p.a_scale + row), __ldg(p.b_scale + x.g)) : 0.0f;
+            // scales are fetched before the wait so their latency hides under the MMAs
+            const float sa = valid ? __ldg(p.a_scale + row) : 0.0f;
+            const float sbw = __ldg(p.b_scale + x.g);
+            const float prob = (valid && p.row_prob) ? __ldg(p.row_prob + row) : 1.0f;
+            if (!mbar_wait_bounded(smem_u32(&s.tmem_full), acc_phase, abort, p.err)) break;
+            tc_fence_after();
+            uint32_t v[64];
             if (p.mode == 0) {
-#pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
-                    const int col = h * 128 + c * 32;
-                    uint32_t v[32];
-                    tmem_ld32(lane_addr + ACC_COL + col, v);
-                    tmem_ld_wait();
-                    float y[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) y[j] = __uint_as_float(v[j]) * scale;
-                    if (valid) store_bf16x32(p.out + row * p.ldo + x.nt * BN + col, y);
-                }
+                tmem_ld32(lane_addr + ACC_COL + cg * 64, v);
+                tmem_ld32(lane_addr + ACC_COL + cg * 64 + 32, v + 32);
             } else {
-                const float prob = (valid && p.row_prob) ? __ldg(p.row_prob + row) : 1.0f;
-                float m = 0.0f;
-#pragma unroll 1
-                for (int c = 0; c < 2; ++c) {
-                    const int col = h * 64 + c * 32;
-                    uint32_t vg[32], vu[32];
-                    tmem_ld32(lane_addr + ACC_COL + col, vg);
-                    tmem_ld32(lane_addr + ACC_COL + 128 + col, vu);
-                    tmem_ld_wait();
-                    float d[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float g = __uint_as_float(vg[j]) * scale;
-                        const float u = __uint_as_float(vu[j]) * scale;
-                        float dv = swiglu1(g, u);
-                        if (p.row_prob) dv *= prob;
-                        const float db = __bfloat162float(__float2bfloat16_rn(dv));
-                        m = fmaxf(m, fabsf(db));
-                        d[j] = dv;
-                        vg[j] = __float_as_uint(g);
-                        vu[j] = __float_as_uint(u);
-                    }
-                    if (valid) {
-                        store_bf16x32(p.out + row * p.ldo + x.nt * 128 + col, d);
-                        if (p.c_debug) {
-                            float* cg = p.c_debug + row * p.N + x.nt * 128 + col;
-                            float* cu = p.c_debug + row * p.N + p.N / 2 + x.nt * 128 + col;
-#pragma unroll
-                            for (int j = 0; j < 32; j += 4) {
-                                *reinterpret_cast<float4*>(cg + j) = make_float4(
-                                    __uint_as_float(vg[j]), __uint_as_float(vg[j + 1]),
-                                    __uint_as_float(vg[j + 2]), __uint_as_float(vg[j + 3]));
-                                *reinterpret_cast<float4*>(cu + j) = make_float4(
-                                    __uint_as_float(vu[j]), __uint_as_float(vu[j + 1]),
-                                    __uint_as_float(vu[j + 2]), __uint_as_float(vu[j + 3]));
-                            }
-                        }
-                    }
-                }
-                if (valid) atomicMax(reinterpret_cast<unsigned int*>(p.amax_out + row), __float_as_uint(m));
+                tmem_ld32(lane_addr + ACC_COL + cg * 32, v);             // gate
+                tmem_ld32(lane_addr + ACC_COL + 128 + cg * 32, v + 32);  // up
             }
+            tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&s.tmem_empty));
             acc_phase ^= 1;
+            if (!valid) continue;
+            const float scale = __fmul_rn(sa, sbw);
+            if (p.mode == 0) {
+                uint4* dst = reinterpret_cast<uint4*>(p.out + row * p.ldo + x.nt * BN + cg * 64);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const float* f = reinterpret_cast<const float*>(v + c * 8);
+                    dst[c] = make_uint4(pack_bf16(f[0] * scale, f[1] * scale), pack_bf16(f[2] * scale, f[3] * scale),
+                                        pack_bf16(f[4] * scale, f[5] * scale), pack_bf16(f[6] * scale, f[7] * scale));
+                }
+            } else {
+                uint4* dst = reinterpret_cast<uint4*>(p.out + row * p.ldo + x.nt * 128 + cg * 32);
+                float m = 0.0f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float d[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float g = __uint_as_float(v[c * 8 + j]) * scale;
+                        const float u = __uint_as_float(v[32 + c * 8 + j]) * scale;
+                        float dv = silu(g) * u;
+                        if (p.row_prob) dv *= prob;
+                        m = fmaxf(m, fabsf(dv));
+                        d[j] = dv;
+                    }
+                    dst[c] = make_uint4(pack_bf16(d[0], d[1]), pack_bf16(d[2], d[3]), pack_bf16(d[4], d[5]),
+                                        pack_bf16(d[6], d[7]));
+                }
+                if (p.c_debug) {
+                    float* cgp = p.c_debug + row * p.N + x.nt * 128 + cg * 32;
+                    float* cup = cgp + p.N / 2;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        *reinterpret_cast<float4*>(cgp + j) = make_float4(
+                            __uint_as_float(v[j]) * scale, __uint_as_float(v[j + 1]) * scale,
+                            __uint_as_float(v[j + 2]) * scale, __uint_as_float(v[j + 3]) * scale);
+                        *reinterpret_cast<float4*>(cup + j) = make_float4(
+                            __uint_as_float(v[32 + j]) * scale, __uint_as_float(v[33 + j]) * scale,
+                            __uint_as_float(v[34 + j]) * scale, __uint_as_float(v[35 + j]) * scale);
+                    }
+                }
+                // max |bf16(d)| = bf16(max |d|): rounding is monotone and odd
+                const float mb = __bfloat162float(__float2bfloat16_rn(m));
+                atomicMax(reinterpret_cast<unsigned int*>(p.amax_out + row), __float_as_uint(mb));
+            }
         }
     }
     tc_fence_before();
@@ -367,9 +402,12 @@ bool make_codes_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_
 }  // namespace
 
 int device_sm_count() {
+    static int cache[64] = {0};
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) cache[dev] = n;
     return n;
 }
 

@@ -77,7 +77,7 @@ struct RouteLaunch {
     float* amax2;          // zeroed here for the FC1 epilogue ([T*k])
     float* row_w;          // nullable: [T*k] router weight of each expert-ordered row
 };
-constexpr int kRouteChunk = 128;  // tokens per chunk of the stable scatter
+constexpr int kRouteChunk = 32;  // tokens per chunk of the stable scatter (one bitmap word)
 cudaError_t launch_route(const RouteLaunch& r, cudaStream_t stream);
 
 struct CombineLaunch {

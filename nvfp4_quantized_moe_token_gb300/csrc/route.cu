@@ -7,17 +7,18 @@
 // activation travels with its scales through the reorder.  Routing: top-8 of
 // 128 experts ("miniTE Technical Report" 6.4 D15 profiles).
 //
-// Three kernels, all deterministic:
+// Four kernels, all deterministic:
 //   1. route_topk: one warp per token -- z = logit + bias, k rounds of warp
 //      argmax (ties to the lower expert), softmax over the k selected z;
 //      per-chunk expert histogram in shared memory.
 //   2. route_scan: one block per expert scans its chunk counts; the last
 //      block to finish turns the expert totals into offsets and padded
 //      offsets.
-//   3. route_scatter: one block per chunk ranks each (token, slot) inside its
-//      expert by a shared-memory bitmap (stable: ascending token index),
-//      writes perm / inv, and copies the token's codes, scales and outer
-//      scale to every expert row it was routed to.
+//   3. route_scatter: one block per chunk of 32 tokens ranks each (token,
+//      slot) inside its expert by a shared-memory bitmap (stable: ascending
+//      token index) and writes perm / inv.
+//   4. route_permute: one warp per expert-ordered row copies the token's
+//      codes, scales and outer scale into the expert-ordered buffers.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -134,71 +135,64 @@ __global__ void __launch_bounds__(kThreads) route_scan_kernel(RouteLaunch p, int
 }
 
 __global__ void __launch_bounds__(kThreads) route_scatter_kernel(RouteLaunch p) {
-    extern __shared__ int smem[];
+    // one chunk of 32 tokens: bit t of bitmap[e] says token t of the chunk chose e
+    extern __shared__ uint32_t bitmap[];
     const int E = p.E, k = p.k;
     const int nslot = kRouteChunk * k;
-    uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem);   // [E][kRouteChunk/32]
-    int* sid = smem + E * (kRouteChunk / 32);                // [nslot] expert ids
-    int* spos = sid + nslot;                                 // [nslot] expert-ordered row
-    int* sprow = spos + nslot;                               // [nslot] padded scale row
     const int64_t t0 = (int64_t)blockIdx.x * kRouteChunk;
-    for (int i = threadIdx.x; i < E * (kRouteChunk / 32); i += kThreads) bitmap[i] = 0u;
+    for (int i = threadIdx.x; i < E; i += kThreads) bitmap[i] = 0u;
     __syncthreads();
     for (int i = threadIdx.x; i < nslot; i += kThreads) {
         const int tl = i / k;
-        const int64_t t = t0 + tl;
-        int e = -1;
-        if (t < p.T) {
-            e = p.ids[t0 * k + i];
-            if (e < 0 || e >= E) { atomicOr(p.err, NVFP4_DEVERR_BADEXPERT); e = -1; }
-            else atomicOr(&bitmap[e * (kRouteChunk / 32) + (tl >> 5)], 1u << (tl & 31));
-        }
-        sid[i] = e;
+        if (t0 + tl >= p.T) continue;
+        const int e = p.ids[t0 * k + i];
+        if (e < 0 || e >= E) atomicOr(p.err, NVFP4_DEVERR_BADEXPERT);
+        else atomicOr(&bitmap[e], 1u << tl);
     }
     __syncthreads();
     for (int i = threadIdx.x; i < nslot; i += kThreads) {
-        const int e = sid[i];
-        if (e < 0) continue;
         const int tl = i / k;
-        const uint32_t* bm = bitmap + e * (kRouteChunk / 32);
-        int rank = __popc(bm[tl >> 5] & ((1u << (tl & 31)) - 1u));
-        for (int w = 0; w < (tl >> 5); ++w) rank += __popc(bm[w]);
-        const int off = __ldg(p.off + e);
-        const int pos = off + p.chunk_base[(int64_t)blockIdx.x * E + e] + rank;
+        if (t0 + tl >= p.T) continue;
         const int64_t ts = t0 * k + i;  // = t * k + slot
+        const int e = p.ids[ts];
+        if (e < 0 || e >= E) continue;
+        const int rank = __popc(bitmap[e] & ((1u << tl) - 1u));
+        const int pos = __ldg(p.off + e) + p.chunk_base[(int64_t)blockIdx.x * E + e] + rank;
         p.perm[pos] = (int)ts;
         p.inv[ts] = pos;
         p.amax2[pos] = 0.0f;
         if (p.row_w) p.row_w[pos] = p.w[ts];
-        spos[i] = pos;
-        sprow[i] = __ldg(p.poff + e) + (pos - off);
     }
+}
+
+// Permute: one warp per expert-ordered row r copies the codes, the block
+// scales (into the 128-row-padded layout of its expert) and the outer scale
+// of token perm[r] / k.
+__global__ void __launch_bounds__(kThreads) route_permute_kernel(RouteLaunch p, int64_t R) {
+    __shared__ int soff[257], spoff[257];
+    const int E = p.E;
+    for (int i = threadIdx.x; i <= E; i += kThreads) { soff[i] = __ldg(p.off + i); spoff[i] = __ldg(p.poff + i); }
     __syncthreads();
-    // copy each token's quantized row to its k expert rows
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t row_bytes = p.H / 2;
-    const int64_t sp4 = p.H / 64;  // scale-column groups per row
-    for (int tl = warp; tl < kRouteChunk; tl += kWarps) {
-        const int64_t t = t0 + tl;
-        if (t >= p.T) break;
-        const uint8_t* src = p.xq_codes + t * row_bytes;
-        for (int64_t c = lane * 16; c < row_bytes; c += 512) {
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + c));
-            for (int s = 0; s < k; ++s) {
-                const int pos = spos[tl * k + s];
-                if (pos >= 0 && sid[tl * k + s] >= 0)
-                    *reinterpret_cast<uint4*>(p.a1_codes + (int64_t)pos * row_bytes + c) = v;
-            }
-        }
-        for (int64_t q = lane; q < sp4; q += 32) {
-            const uint32_t g = __ldg(reinterpret_cast<const uint32_t*>(p.xq_sf + sf_group_offset(t, q, sp4)));
-            for (int s = 0; s < k; ++s) {
-                if (sid[tl * k + s] < 0) continue;
-                *reinterpret_cast<uint32_t*>(p.a1_sf + sf_group_offset(sprow[tl * k + s], q, sp4)) = g;
-            }
-        }
-        if (lane < k && sid[tl * k + lane] >= 0) p.a1_scale[spos[tl * k + lane]] = __ldg(p.xq_scale + t);
+    const int lane = threadIdx.x & 31;
+    const int64_t r = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+    if (r >= R) return;
+    int lo = 0, hi = E;  // expert e with off[e] <= r < off[e+1]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (soff[mid] <= r) lo = mid; else hi = mid;
     }
+    const int64_t prow = spoff[lo] + (r - soff[lo]);
+    const int64_t t = __ldg(p.perm + r) / p.k;
+    const int64_t row_bytes = p.H / 2;
+    const uint8_t* src = p.xq_codes + t * row_bytes;
+    uint8_t* dst = p.a1_codes + r * row_bytes;
+    for (int64_t c = lane * 16; c < row_bytes; c += 512)
+        *reinterpret_cast<uint4*>(dst + c) = __ldg(reinterpret_cast<const uint4*>(src + c));
+    const int64_t sp4 = p.H / 64;
+    for (int64_t q = lane; q < sp4; q += 32)
+        *reinterpret_cast<uint32_t*>(p.a1_sf + sf_group_offset(prow, q, sp4)) =
+            __ldg(reinterpret_cast<const uint32_t*>(p.xq_sf + sf_group_offset(t, q, sp4)));
+    if (lane == 0) p.a1_scale[r] = __ldg(p.xq_scale + t);
 }
 
 }  // namespace
@@ -221,8 +215,11 @@ cudaError_t launch_route(const RouteLaunch& r, cudaStream_t stream) {
     route_scan_kernel<<<r.E, kThreads, 0, stream>>>(r, nchunks);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const size_t smem = sizeof(int) * ((size_t)r.E * (kRouteChunk / 32) + 3 * (size_t)kRouteChunk * r.k);
-    route_scatter_kernel<<<nchunks, kThreads, smem, stream>>>(r);
+    route_scatter_kernel<<<nchunks, kThreads, sizeof(uint32_t) * r.E, stream>>>(r);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int64_t R = r.T * r.k;
+    route_permute_kernel<<<(unsigned)((R + kThreads / 32 - 1) / (kThreads / 32)), kThreads, 0, stream>>>(r, R);
     return cudaGetLastError();
 }
 
