@@ -8,11 +8,11 @@
 // concurrently across CTAs).
 //
 // Persistent kernel, one CTA per SM, 22 warps with fixed roles:
-//   warp 0       TMA producer: per K-stage the A tile (128 rows x 256 FP4,
-//                128B-swizzled), the B tile (256 rows: two 128-row boxes) and
+//   warp 0       TMA producer: per K-stage the A tile (128 rows x 128 FP4,
+//                64B-swizzled), the B tile (256 rows: two 128-row boxes) and
 //                the E4M3 scale atoms of both (plain bulk copies: the
-//                quantizer wrote them in the MMA's layout), 4-stage ring.
-//   warp 1       TMEM allocator and MMA issuer: per stage four
+//                quantizer wrote them in the MMA's layout), 6-stage ring.
+//   warp 1       TMEM allocator and MMA issuer: per stage two
 //                tcgen05.mma.kind::mxf4nvf4.block_scale (M=128, N=256,
 //                K=64), fp32 accumulation in TMEM; tcgen05.commit frees the
 //                smem stage and, after the last stage, hands the accumulator
@@ -24,8 +24,12 @@
 //                three of them per MMA; tcgen05.st runs on the warps.)
 //   warps 6-21   epilogue: each warp copies its 32 rows x 64 accumulator
 //                columns into registers, releases TMEM at once (the next
-//                tile's MMAs start), then scales and either stores bf16
+//                tile's MMAs start), then scales and either converts to bf16
 //                (mode 0) or computes SwiGLU -> bf16 D + row amax (mode 1).
+//                Outputs leave through a per-warp shared-memory box of 32
+//                rows x 32 columns and a TMA tensor store (coalesced, off the
+//                warps); a warp whose 32 rows straddle the end of an expert
+//                group stores its valid rows directly instead.
 // Tiles are ordered (padded m-tile, n-tile) with n fastest, so CTAs running
 // at the same time share the A rows and one expert's weights in L2.
 // Every pipeline wait is bounded in time; a wait that runs out raises an
@@ -44,31 +48,50 @@ namespace {
 
 constexpr int BM = 128;                 // rows per tile (TMEM lanes)
 constexpr int BN = 256;                 // accumulator columns per tile
-constexpr int BK = 256;                 // FP4 elements of K per stage (128 bytes)
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK / 2;    // 16 KB
-constexpr int B_BYTES = BN * BK / 2;    // 32 KB
-constexpr int ATOMS = BK / 64;          // scale atoms (128 rows x 4 scales) per 128 rows per stage
-constexpr int SFA_BYTES = ATOMS * 512;  // 2 KB
-constexpr int SFB_BYTES = 2 * ATOMS * 512;
-constexpr int EPI_WARP0 = 6;            // warps 6..21 run the epilogue (2..5 write scales)
+constexpr int EPI_WARP0 = 6;            // warps 2..5 write scales, 6..21 run the epilogue
 constexpr int EPI_WARPS = 16;
 constexpr int THREADS = (EPI_WARP0 + EPI_WARPS) * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;
-constexpr uint32_t SF_COL = 256;        // per stage: SFA 4 atoms x 4 cols, SFB 8 atoms x 4 cols
-constexpr uint32_t SF_STAGE_COLS = 48;
+constexpr uint32_t SF_COL = 256;
 constexpr int MAX_G = 256;
 constexpr uint32_t IDESC = idesc_nvfp4(BM, BN);
+constexpr int STG_BYTES = 32 * 64;      // per-warp output staging box: 32 rows x 32 bf16
 
+// Pipeline shape per epilogue mode.  The plain (mode 0) epilogue writes a
+// full 128 x 256 bf16 tile per K loop of at most a few stages (FC2: K = 768),
+// so it takes 64-byte K-stages (6 in flight) and leaves room for the TMA-store
+// staging boxes.  The SwiGLU (mode 1) epilogue writes half as much per much
+// longer K loop (FC1: K = 2048): it keeps 128-byte K-stages (4 in flight,
+// more bytes per TMA request) and stores directly.
+template <int MODE>
+struct Cfg {
+    static constexpr int BK = MODE == 0 ? 128 : 256;    // FP4 elements of K per stage
+    static constexpr int ROWB = BK / 2;                 // bytes per row per stage
+    static constexpr int STAGES = MODE == 0 ? 6 : 4;
+    static constexpr int A_BYTES = BM * ROWB;
+    static constexpr int B_BYTES = BN * ROWB;
+    static constexpr int ATOMS = BK / 64;               // scale atoms per 128 rows per stage
+    static constexpr int SFA_BYTES = ATOMS * 512;
+    static constexpr int SFB_BYTES = 2 * ATOMS * 512;
+    static constexpr int SWZ = MODE == 0 ? 4 : 2;       // descriptor swizzle code: 64B / 128B
+    static constexpr int SBO = 8 * ROWB;                // bytes between 8-row core-matrix groups
+    static constexpr uint32_t SF_STAGE_COLS = 12 * ATOMS;  // SFA 4*ATOMS + SFB 8*ATOMS columns
+    static constexpr bool STAGED = MODE == 0;
+    static constexpr int NSTG = STAGED ? EPI_WARPS : 0;
+};
+
+template <int MODE>
 struct __align__(1024) Smem {
-    uint8_t a[STAGES][A_BYTES];
-    uint8_t b[STAGES][B_BYTES];
-    uint8_t sfa[STAGES][SFA_BYTES];
-    uint8_t sfb[STAGES][SFB_BYTES];
-    uint64_t full[STAGES];      // TMA bytes landed
-    uint64_t sf_full[STAGES];   // scales of the stage written to TMEM (4 warps)
-    uint64_t empty[STAGES];     // MMAs of the stage done (commit)
+    using C = Cfg<MODE>;
+    uint8_t a[C::STAGES][C::A_BYTES];
+    uint8_t b[C::STAGES][C::B_BYTES];
+    uint8_t sfa[C::STAGES][C::SFA_BYTES];
+    uint8_t sfb[C::STAGES][C::SFB_BYTES];
+    uint8_t stg[C::NSTG > 0 ? C::NSTG : 1][C::NSTG > 0 ? STG_BYTES : 16];
+    uint64_t full[C::STAGES];      // TMA bytes landed
+    uint64_t sf_full[C::STAGES];   // scales of the stage written to TMEM (4 warps)
+    uint64_t empty[C::STAGES];     // MMAs of the stage done (commit)
     uint64_t tmem_full;
     uint64_t tmem_empty;
     uint64_t drain;
@@ -101,7 +124,8 @@ struct Tile {
     int g, row0, rows, mt, nt;
 };
 
-__device__ __forceinline__ Tile decode_tile(const Smem& s, int G, int n_tiles, int t) {
+template <class S>
+__device__ __forceinline__ Tile decode_tile(const S& s, int G, int n_tiles, int t) {
     Tile x;
     x.mt = t / n_tiles;
     x.nt = t - x.mt * n_tiles;
@@ -123,6 +147,36 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// One warp's 32 rows x 32 bf16 output columns (16 packed words per thread,
+// thread = row).  Whole warp inside the group: stage the box in shared memory
+// (64B-swizzled, as the tensor map expects) and issue one TMA tensor store;
+// otherwise each valid row is stored directly.
+template <bool STAGED>
+__device__ __forceinline__ void emit_box(const KParams& p, const CUtensorMap* tmO, uint32_t stg, const uint32_t* w,
+                                         bool full_warp, bool valid, int lane, int64_t row, int col, int row_base) {
+    if (STAGED && full_warp) {
+        if (lane == 0) bulk_wait_read();  // the previous box of this warp has been read
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t a = stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                         :: "r"(a), "r"(w[4 * c]), "r"(w[4 * c + 1]), "r"(w[4 * c + 2]), "r"(w[4 * c + 3])
+                         : "memory");
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tmO, stg, col, row_base);
+            bulk_commit();
+        }
+    } else if (valid) {
+        uint4* dst = reinterpret_cast<uint4*>(p.out + row * p.ldo + col);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) dst[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+    }
+}
+
 // silu(g) = g / (1 + exp(-g)) with the hardware exp2 and reciprocal
 // approximations (a few fp32 ulps, far inside the bf16 rounding that follows);
 // exp(-g) = inf for very negative g gives rcp = 0 and silu = -0, no NaN.
@@ -130,11 +184,16 @@ __device__ __forceinline__ float silu(float g) {
     return g * rcp_approx(1.0f + __expf(-g));
 }
 
+template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                  const KParams p) {
+                  const __grid_constant__ CUtensorMap tmO, const KParams p) {
+    using C = Cfg<MODE>;
+    constexpr int STAGES = C::STAGES, A_BYTES = C::A_BYTES, B_BYTES = C::B_BYTES, ATOMS = C::ATOMS;
+    constexpr int SFB_BYTES = C::SFB_BYTES, ROWB = C::ROWB, SWZ = C::SWZ, SBO = C::SBO;
+    constexpr uint32_t SF_STAGE_COLS = C::SF_STAGE_COLS;
     extern __shared__ uint8_t smem_raw[];
-    Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Smem<MODE>& s = *reinterpret_cast<Smem<MODE>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.G;
 
@@ -160,7 +219,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         s.consumed = 0;
         fence_barrier_init();
     }
-    if (warp == 0 && lane == 0) { prefetch_tmap(&tmA); prefetch_tmap(&tmB); }
+    if (warp == 0 && lane == 0) { prefetch_tmap(&tmA); prefetch_tmap(&tmB); prefetch_tmap(&tmO); }
     if (warp == 1) { tmem_alloc(smem_u32(&s.tmem_base), TMEM_COLS); tmem_relinquish(); }
     tc_fence_before();
     __syncthreads();
@@ -168,7 +227,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const uint32_t tmem = s.tmem_base;
     volatile int* abort = &s.abort;
 
-    const int n_tiles = p.mode == 1 ? p.N / 256 : p.N / BN;  // mode 1: 128 gate + 128 up columns per tile
+    const int n_tiles = MODE == 1 ? p.N / 256 : p.N / BN;  // mode 1: 128 gate + 128 up columns per tile
     const int total = (s.gpoff[G] / BM) * n_tiles;
     const int k_atoms = p.K / 64;
     const int k_stages = (k_atoms + ATOMS - 1) / ATOMS;
@@ -184,16 +243,16 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const Tile x = decode_tile(s, G, n_tiles, t);
-                const int jb0 = p.mode == 1 ? x.g * (p.N / 128) + x.nt : x.g * (p.N / 128) + 2 * x.nt;
-                const int jb1 = p.mode == 1 ? x.g * (p.N / 128) + p.N / 256 + x.nt : jb0 + 1;
+                const int jb0 = MODE == 1 ? x.g * (p.N / 128) + x.nt : x.g * (p.N / 128) + 2 * x.nt;
+                const int jb1 = MODE == 1 ? x.g * (p.N / 128) + p.N / 256 + x.nt : jb0 + 1;
                 for (int ks = 0; ks < k_stages; ++ks) {
                     if (!mbar_wait_bounded(smem_u32(&s.empty[stage]), phase ^ 1, abort, p.err)) { ok = false; break; }
                     const int na = k_atoms - ks * ATOMS < ATOMS ? k_atoms - ks * ATOMS : ATOMS;
                     const uint32_t fb = smem_u32(&s.full[stage]);
                     mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES + 3 * na * 512);
-                    tma_load_2d(smem_u32(s.a[stage]), &tmA, fb, ks * 128, x.row0);
-                    tma_load_2d(smem_u32(s.b[stage]), &tmB, fb, ks * 128, jb0 * 128);
-                    tma_load_2d(smem_u32(s.b[stage]) + B_BYTES / 2, &tmB, fb, ks * 128, jb1 * 128);
+                    tma_load_2d(smem_u32(s.a[stage]), &tmA, fb, ks * ROWB, x.row0);
+                    tma_load_2d(smem_u32(s.b[stage]), &tmB, fb, ks * ROWB, jb0 * 128);
+                    tma_load_2d(smem_u32(s.b[stage]) + B_BYTES / 2, &tmB, fb, ks * ROWB, jb1 * 128);
                     bulk_load(smem_u32(s.sfa[stage]), p.a_sf + ((int64_t)x.mt * k_atoms + ks * ATOMS) * 512, na * 512, fb);
                     bulk_load(smem_u32(s.sfb[stage]), p.b_sf + ((int64_t)jb0 * k_atoms + ks * ATOMS) * 512, na * 512, fb);
                     bulk_load(smem_u32(s.sfb[stage]) + SFB_BYTES / 2,
@@ -231,9 +290,9 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     const uint32_t sfc = tmem + SF_COL + stage * SF_STAGE_COLS;
                     const uint32_t a0 = smem_u32(s.a[stage]), b0 = smem_u32(s.b[stage]);
                     for (int kk = 0; kk < na; ++kk) {
-                        tc_mma_nvfp4(tmem + ACC_COL, smem_desc(a0 + kk * 32, 0, 1024, 2),
-                                     smem_desc(b0 + kk * 32, 0, 1024, 2), IDESC,
-                                     sfc + kk * 4, sfc + 16 + kk * 8, (ks | kk) != 0);
+                        tc_mma_nvfp4(tmem + ACC_COL, smem_desc(a0 + kk * 32, 0, SBO, SWZ),
+                                     smem_desc(b0 + kk * 32, 0, SBO, SWZ), IDESC,
+                                     sfc + kk * 4, sfc + 4 * ATOMS + kk * 8, (ks | kk) != 0);
                     }
                     tc_commit(smem_u32(&s.empty[stage]));
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -252,7 +311,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         // of 16 bytes; line i holds the 4 scales of rows i, i+32, i+64, i+96)
         // goes to 4 consecutive columns of every quarter: thread i of each
         // quarter writes line i.  SFA atom kk -> columns sfc + 4kk; SFB atom kk
-        // of half hh -> columns sfc + 16 + 8kk + 4hh.
+        // of half hh -> columns sfc + 4*ATOMS + 8kk + 4hh.
         const int q = warp & 3;
         const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
         int stage = 0;
@@ -268,8 +327,8 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     const uint4 b0 = *reinterpret_cast<const uint4*>(s.sfb[stage] + kk * 512 + lane * 16);
                     const uint4 b1 = *reinterpret_cast<const uint4*>(s.sfb[stage] + SFB_BYTES / 2 + kk * 512 + lane * 16);
                     tmem_st4(sfc + kk * 4, a.x, a.y, a.z, a.w);
-                    tmem_st4(sfc + 16 + kk * 8, b0.x, b0.y, b0.z, b0.w);
-                    tmem_st4(sfc + 20 + kk * 8, b1.x, b1.y, b1.z, b1.w);
+                    tmem_st4(sfc + 4 * ATOMS + kk * 8, b0.x, b0.y, b0.z, b0.w);
+                    tmem_st4(sfc + 4 * ATOMS + 4 + kk * 8, b1.x, b1.y, b1.z, b1.w);
                 }
                 tmem_st_wait();
                 tc_fence_before();
@@ -299,7 +358,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             if (!mbar_wait_bounded(smem_u32(&s.tmem_full), acc_phase, abort, p.err)) break;
             tc_fence_after();
             uint32_t v[64];
-            if (p.mode == 0) {
+            if (MODE == 0) {
                 tmem_ld32(lane_addr + ACC_COL + cg * 64, v);
                 tmem_ld32(lane_addr + ACC_COL + cg * 64 + 32, v + 32);
             } else {
@@ -311,35 +370,21 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&s.tmem_empty));
             acc_phase ^= 1;
-            if (!valid) continue;
             const float scale = __fmul_rn(sa, sbw);
-            if (p.mode == 0) {
-                uint4* dst = reinterpret_cast<uint4*>(p.out + row * p.ldo + x.nt * BN + cg * 64);
+            // all 32 rows of this warp inside the tile's group: TMA store; else direct
+            const bool full_warp = q * 32 + 32 <= x.rows;
+            const uint32_t stg = smem_u32(s.stg[C::NSTG > 0 ? warp - EPI_WARP0 : 0]);
+            if (MODE == 0) {
+                uint32_t w[32];  // convert all 64 values first: the fp32 registers die as they are packed
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const float* f = reinterpret_cast<const float*>(v + c * 8);
-                    dst[c] = make_uint4(pack_bf16(f[0] * scale, f[1] * scale), pack_bf16(f[2] * scale, f[3] * scale),
-                                        pack_bf16(f[4] * scale, f[5] * scale), pack_bf16(f[6] * scale, f[7] * scale));
-                }
+                for (int j = 0; j < 32; ++j)
+                    w[j] = pack_bf16(__uint_as_float(v[2 * j]) * scale, __uint_as_float(v[2 * j + 1]) * scale);
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf)
+                    emit_box<C::STAGED>(p, &tmO, stg, w + hf * 16, full_warp, valid, lane, row,
+                                        x.nt * BN + cg * 64 + hf * 32, x.row0 + q * 32);
             } else {
-                uint4* dst = reinterpret_cast<uint4*>(p.out + row * p.ldo + x.nt * 128 + cg * 32);
-                float m = 0.0f;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float d[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float g = __uint_as_float(v[c * 8 + j]) * scale;
-                        const float u = __uint_as_float(v[32 + c * 8 + j]) * scale;
-                        float dv = silu(g) * u;
-                        if (p.row_prob) dv *= prob;
-                        m = fmaxf(m, fabsf(dv));
-                        d[j] = dv;
-                    }
-                    dst[c] = make_uint4(pack_bf16(d[0], d[1]), pack_bf16(d[2], d[3]), pack_bf16(d[4], d[5]),
-                                        pack_bf16(d[6], d[7]));
-                }
-                if (p.c_debug) {
+                if (valid && p.c_debug) {
                     float* cgp = p.c_debug + row * p.N + x.nt * 128 + cg * 32;
                     float* cup = cgp + p.N / 2;
 #pragma unroll
@@ -352,11 +397,32 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                             __uint_as_float(v[34 + j]) * scale, __uint_as_float(v[35 + j]) * scale);
                     }
                 }
+                uint32_t w[16];
+                float m = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    float d2[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float g = __uint_as_float(v[2 * j + e]) * scale;
+                        const float u = __uint_as_float(v[32 + 2 * j + e]) * scale;
+                        float dv = silu(g) * u;
+                        if (p.row_prob) dv *= prob;
+                        m = fmaxf(m, fabsf(dv));
+                        d2[e] = dv;
+                    }
+                    w[j] = pack_bf16(d2[0], d2[1]);
+                }
+                emit_box<C::STAGED>(p, &tmO, stg, w, full_warp, valid, lane, row, x.nt * 128 + cg * 32, x.row0 + q * 32);
                 // max |bf16(d)| = bf16(max |d|): rounding is monotone and odd
-                const float mb = __bfloat162float(__float2bfloat16_rn(m));
-                atomicMax(reinterpret_cast<unsigned int*>(p.amax_out + row), __float_as_uint(mb));
+                if (valid) {
+                    const float mb = __bfloat162float(__float2bfloat16_rn(m));
+                    atomicMax(reinterpret_cast<unsigned int*>(p.amax_out + row), __float_as_uint(mb));
+                }
             }
         }
+        if (C::STAGED && lane == 0) bulk_wait_all();  // this warp's tensor stores are complete before exit
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -386,16 +452,31 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 2D uint8 view [rows x row_bytes] of packed FP4 codes, 128-byte x 128-row boxes, 128B swizzle.
-bool make_codes_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes) {
+// 2D uint8 view [rows x row_bytes] of packed FP4 codes: boxes of ROWB bytes x
+// 128 rows, swizzled to match the MMA descriptors of the mode.
+bool make_codes_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes, int mode) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
+    const int rowb = mode == 0 ? Cfg<0>::ROWB : Cfg<1>::ROWB;
     cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-    cuuint32_t box[2] = {128, 128};
+    cuuint32_t box[2] = {(cuuint32_t)rowb, 128};
     cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, rowb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2D bf16 view [rows x cols] (row stride ld elements) of an output, 32 x 32 boxes, 64B swizzle.
+bool make_out_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -413,9 +494,11 @@ int device_sm_count() {
 
 cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
     if (g.M <= 0) return cudaSuccess;
-    CUtensorMap ta, tb;
-    if (!make_codes_map(&ta, g.a_codes, g.M, g.K / 2)) return cudaErrorInvalidValue;
-    if (!make_codes_map(&tb, g.b_codes, (int64_t)g.G * g.N, g.K / 2)) return cudaErrorInvalidValue;
+    CUtensorMap ta, tb, to;
+    if (!make_codes_map(&ta, g.a_codes, g.M, g.K / 2, g.mode)) return cudaErrorInvalidValue;
+    if (!make_codes_map(&tb, g.b_codes, (int64_t)g.G * g.N, g.K / 2, g.mode)) return cudaErrorInvalidValue;
+    const int64_t out_cols = g.mode == 1 ? g.N / 2 : g.N;
+    if (!make_out_map(&to, g.out, g.M, out_cols, g.ldo)) return cudaErrorInvalidValue;
     KParams p;
     p.a_sf = g.a_sf;
     p.a_scale = g.a_scale;
@@ -434,19 +517,30 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
     p.row_prob = g.row_prob;
     p.c_debug = g.c_debug;
     p.err = g.err;
-    const size_t smem = sizeof(Smem) + 1024;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [&] {
-        attr_err = cudaFuncSetAttribute(gemm_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
     int grid = g.num_sms > 0 ? g.num_sms : 148;
     if (g.goff == nullptr) {
         const int64_t tiles = (g.M + BM - 1) / BM * (g.N / BN);
         if (tiles < grid) grid = (int)tiles;
     }
-    gemm_nvfp4_kernel<<<grid, THREADS, smem, stream>>>(ta, tb, p);
+    if (g.mode == 0) {
+        const size_t smem = sizeof(Smem<0>) + 1024;
+        static std::once_flag once0;
+        static cudaError_t err0 = cudaSuccess;
+        std::call_once(once0, [&] {
+            err0 = cudaFuncSetAttribute(gemm_nvfp4_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        });
+        if (err0 != cudaSuccess) return err0;
+        gemm_nvfp4_kernel<0><<<grid, THREADS, smem, stream>>>(ta, tb, to, p);
+    } else {
+        const size_t smem = sizeof(Smem<1>) + 1024;
+        static std::once_flag once1;
+        static cudaError_t err1 = cudaSuccess;
+        std::call_once(once1, [&] {
+            err1 = cudaFuncSetAttribute(gemm_nvfp4_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        });
+        if (err1 != cudaSuccess) return err1;
+        gemm_nvfp4_kernel<1><<<grid, THREADS, smem, stream>>>(ta, tb, to, p);
+    }
     return cudaGetLastError();
 }
 
