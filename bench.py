@@ -54,6 +54,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--quick", action="store_true", help="profiling runs: no e2e, no oracle, no clocks")
+    p.add_argument("--only", choices=["all", "quant"], default="all",
+                   help="quant: time only the 16384 x 2048 quantizer workload (for profiling)")
     return p.parse_args()
 
 
@@ -208,10 +210,12 @@ def run_ours(args, rank, world, local):
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("timed")
     for i in range(args.steps):
         flush.zero_()
         step(events[i])
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     barrier(world)
     step_ms = [ev[0].elapsed_time(ev[-1]) for ev in events]
     stage_ms = {s: [ev[j].elapsed_time(ev[j + 1]) for ev in events] for j, s in enumerate(nv.STAGES)}
@@ -287,7 +291,7 @@ def run_ours(args, rank, world, local):
     return res, d
 
 
-def quant_gbs(args, local):
+def quant_gbs(args, local, reps=50):
     """Quantizer throughput on the 16384 x 2048 per-token workload (L2 flushed per rep)."""
     import nvfp4_quantized_moe_token_gb300 as nv
     dev = torch.device("cuda", local)
@@ -298,7 +302,9 @@ def quant_gbs(args, local):
     for _ in range(5):
         nv.quantize_rows(x, out=q)
     ts = []
-    for _ in range(50):
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("timed_quant")
+    for _ in range(reps):
         flush.zero_()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
@@ -306,6 +312,7 @@ def quant_gbs(args, local):
         b.record()
         ts.append((a, b))
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     ms = statistics.fmean(a.elapsed_time(b) for a, b in ts)
     nbytes = 16384 * (2048 * 2 + 1024 + 128 + 4)
     return {"workload": "quantize 16384 x 2048", "us": ms * 1e3, "gbs": nbytes / (ms / 1e3) / 1e9,
@@ -388,6 +395,10 @@ def main():
         return
     import nvfp4_quantized_moe_token_gb300 as nv
     nv.lib()
+    if args.only == "quant":
+        if rank == 0:
+            print(json.dumps({"quant": quant_gbs(args, local, reps=max(args.steps, 1))}))
+        return
     res, d = run_ours(args, rank, world, local)
     if rank == 0:
         if not args.quick:

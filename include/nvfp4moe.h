@@ -41,8 +41,9 @@
  *     an inconsistency (or a pipeline wait that exceeds its time limit)
  *     ORs a bit into a device error word and returns.  The error word is
  *     the first uint32 of `ws` for nvfp4_linear (when ws_bytes >= 4) and
- *     the `err` slot of moe_expert_forward's workspace.  The library never
- *     clears it: the caller zeroes it and reads it when convenient.
+ *     nvfp4_quantize_rows (when ws_bytes >= 16), and the `err` slot of
+ *     moe_expert_forward's workspace.  The library never clears it: the
+ *     caller zeroes it and reads it when convenient.
  */
 #ifndef NVFP4MOE_H
 #define NVFP4MOE_H
@@ -72,7 +73,7 @@ extern "C" {
 #define NVFP4_PER_TENSOR 1 /* one fp32 outer scale for the whole matrix */
 
 /* Bits of the device error word. */
-#define NVFP4_DEVERR_TIMEOUT 1u   /* a pipeline wait in the GEMM ran past its limit */
+#define NVFP4_DEVERR_TIMEOUT 1u   /* a pipeline wait (GEMM or quantizer) ran past its limit */
 #define NVFP4_DEVERR_BADEXPERT 2u /* a routed expert id outside [0, E) */
 
 /*
@@ -99,9 +100,9 @@ typedef struct nvfp4_tensor {
  * ceil(rows/128)*128 * ceil(cols/64)*4.  Pure host function. */
 NVFP4_API size_t nvfp4_sf_bytes(int64_t rows, int64_t cols);
 
-/* Workspace bytes nvfp4_quantize_rows needs: 0 for NVFP4_PER_ROW or when
- * amax_in is given, 256 for NVFP4_PER_TENSOR without amax_in (the tensor
- * amax is reduced there).  Pure host function. */
+/* Workspace bytes nvfp4_quantize_rows needs: 0 for NVFP4_PER_ROW, 256 for
+ * NVFP4_PER_TENSOR (the tensor amax is reduced there when amax_in is not
+ * given).  Pure host function. */
 NVFP4_API size_t nvfp4_quantize_workspace(int64_t rows, int64_t cols, int scale_mode);
 
 /*
@@ -119,10 +120,13 @@ NVFP4_API size_t nvfp4_quantize_workspace(int64_t rows, int64_t cols, int scale_
  *          an fp32 subnormal); code = E2M1_rne_saturating(v), sign kept.
  * Every step is an IEEE fp32 operation in that order, so the result is
  * bit-identical to any implementation of the same steps.
- * Shapes: rows >= 0, cols > 0, cols % 16 == 0, ld >= cols.
+ * Shapes: rows >= 0, 0 < cols <= 32768, cols % 16 == 0, ld >= cols.
  * Alignment: x and ld*2 bytes 16-byte aligned; codes 16-byte aligned.
- * Scale-factor padding rows/columns (beyond rows or cols/16) are not written.
- * ws: nvfp4_quantize_workspace() bytes (may be NULL when that is 0).
+ * Scale-factor padding columns inside the last 4-column group are written 0;
+ * padding rows (beyond rows, up to the 128-row tile) are not written.
+ * ws: nullable when nvfp4_quantize_workspace() is 0.  When ws_bytes >= 16
+ * its first uint32 is the device error word; NVFP4_PER_TENSOR without
+ * amax_in reduces the tensor amax at ws + 16.
  */
 NVFP4_API int nvfp4_quantize_rows(const void* x_bf16, int64_t rows, int64_t cols, int64_t ld,
                         int scale_mode, const float* amax_in, const nvfp4_tensor* out,

@@ -80,13 +80,12 @@ int nvfp4_quantize_rows(const void* x_bf16, int64_t rows, int64_t cols, int64_t 
     if (rows < 0 || cols <= 0 || ld < cols) return fail(NVFP4_EINVAL, "quantize: bad rows/cols/ld");
     if (out->rows != rows || out->cols != cols) return fail(NVFP4_EINVAL, "quantize: out shape mismatch");
     if (cols % 16 != 0) return fail(NVFP4_ESHAPE, "quantize: cols %% 16 != 0 (cols = %lld)", (long long)cols);
-    if (rows >= (1ll << 31) || cols >= (1ll << 24)) return fail(NVFP4_ESHAPE, "quantize: matrix too large");
+    if (rows >= (1ll << 31) || cols > 32768) return fail(NVFP4_ESHAPE, "quantize: rows >= 2^31 or cols > 32768");
     if (!aligned(x_bf16, 16) || (ld % 8) != 0) return fail(NVFP4_EALIGN, "quantize: x and ld*2 must be 16-byte aligned");
     if (amax_in != nullptr && !aligned(amax_in, 4)) return fail(NVFP4_EALIGN, "quantize: amax_in misaligned");
-    if (scale_mode == NVFP4_PER_TENSOR && amax_in == nullptr) {
-        if (ws == nullptr || ws_bytes < 256) return fail(NVFP4_EWORKSPACE, "quantize: per-tensor needs 256 bytes of ws");
-        if (!aligned(ws, 16)) return fail(NVFP4_EALIGN, "quantize: ws must be 16-byte aligned");
-    }
+    if (scale_mode == NVFP4_PER_TENSOR && amax_in == nullptr && (ws == nullptr || ws_bytes < 256))
+        return fail(NVFP4_EWORKSPACE, "quantize: per-tensor needs 256 bytes of ws");
+    if (ws != nullptr && !aligned(ws, 16)) return fail(NVFP4_EALIGN, "quantize: ws must be 16-byte aligned");
     nvfp4::QuantLaunch q{};
     q.x = x_bf16;
     q.ld = ld;
@@ -98,6 +97,7 @@ int nvfp4_quantize_rows(const void* x_bf16, int64_t rows, int64_t cols, int64_t 
     q.sf = out->sf;
     q.scale = out->scale;
     q.ws = ws;
+    q.err = (ws != nullptr && ws_bytes >= 16) ? reinterpret_cast<uint32_t*>(ws) : nullptr;
     cudaError_t e = nvfp4::launch_quantize(q, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(NVFP4_ELAUNCH, "quantize: %s", cudaGetErrorString(e));
     return ok();
@@ -245,6 +245,7 @@ int moe_expert_forward(const void* x_bf16, int64_t T, int64_t H, const float* ro
     qx.codes = at(L.xq_codes);
     qx.sf = at(L.xq_sf);
     qx.scale = reinterpret_cast<float*>(at(L.xq_scale));
+    qx.err = reinterpret_cast<uint32_t*>(at(L.err));
     if ((e = nvfp4::launch_quantize(qx, s)) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe quantize: %s", cudaGetErrorString(e));
     if ((e = mark()) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe event: %s", cudaGetErrorString(e));
 
@@ -317,6 +318,7 @@ int moe_expert_forward(const void* x_bf16, int64_t T, int64_t H, const float* ro
     q2.goff = r.off;
     q2.gpoff = r.poff;
     q2.G = E;
+    q2.err = reinterpret_cast<uint32_t*>(at(L.err));
     if ((e = nvfp4::launch_quantize(q2, s)) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe requant: %s", cudaGetErrorString(e));
     if ((e = mark()) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe event: %s", cudaGetErrorString(e));
 

@@ -19,6 +19,7 @@ struct QuantLaunch {
     const int* gpoff;
     int G;
     void* ws;               // >= 4 bytes when per_tensor && !amax_in
+    uint32_t* err;          // nullable device error word (pipeline wait time-outs)
 };
 cudaError_t launch_quantize(const QuantLaunch& q, cudaStream_t stream);
 

@@ -95,3 +95,18 @@ def test_context_swap_on_device():
     torch.cuda.synchronize()
     assert torch.equal(alone.codes[0].cpu(), inb.codes[20].cpu())
     assert alone.scale[0].item() == inb.scale[20].item()
+
+
+def test_quant_row_scale_sweep():
+    """Rows scaled by 2^k for k across the bf16 exponent range: the per-block
+    division bmax / t meets every binade of t (rows with tiny t take the
+    plain IEEE division, the rest the FMA division with 1/t)."""
+    rng = np.random.default_rng(21)
+    rows, cols = 4096, 512
+    base = rng.standard_normal((rows, cols)).astype(np.float32)
+    base[rng.random((rows, cols)) < 0.05] *= np.float32(37.0)
+    base[rng.random((rows, cols)) < 0.2] *= np.float32(1e-3)
+    k = (np.arange(rows) % 250) - 130
+    x = workloads.to_bf16_bits(base * np.exp2(k).astype(np.float32)[:, None])
+    got, ref = run_both(x)
+    assert_quant_equal(got, ref, rows, cols, what="scale sweep")
