@@ -7,7 +7,7 @@ quantization, permute, FC1 + SwiGLU + row amax, requant, FC2, weighted
 combine -- over one batch of the 32768-token Qwen3-30B-A3B-shaped layer
 (hidden 2048, 128 experts, top-8, FFN 768, router bias ~N(0, 2^2)), with
 seeded synthetic inputs resident in HBM and the weights quantized once
-before timing.  L2 is flushed (256 MiB write) between timed steps, outside
+before timing.  L2 is flushed (256 MiB write, then a 256 MiB read) between timed steps, outside
 the timed region; each step is timed with CUDA events on the launching
 stream, and per-stage events recorded by the library give the kernels'
 durations live.
@@ -40,8 +40,22 @@ T, H, F, E, K_TOP = 32768, 2048, 768, 128, 8
 WORKLOAD = "moe_expert_layer_32k"
 CONFIG = {"workload": WORKLOAD, "tokens": T, "hidden": H, "ffn": F, "experts": E, "topk": K_TOP,
           "router_bias_std": 2.0, "token_expert_rows": T * K_TOP, "weights": "pre-quantized NVFP4, static",
-          "l2": "flushed between timed steps (256 MiB write)", "seed": 3}
+          "l2": "flushed between timed steps (256 MiB write, then a 256 MiB read so no dirty lines remain)",
+          "seed": 3}
 FLUSH_BYTES = 256 << 20
+
+
+class L2Flush:
+    """Write a buffer larger than L2, then read another one: the next timed
+    kernel starts with cold inputs and without dirty lines to write back."""
+
+    def __init__(self, dev):
+        self.w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        self.sink = self.r.sum()
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 : BF16 tensor rate
 
 
@@ -153,6 +167,26 @@ def make_inputs():
     return d
 
 
+def recorded_traffic(stage):
+    """DRAM bytes per launch of a stage's kernel from the committed ncu record,
+    or None when the kernel's sources changed since the counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)["kernels"].get(stage)
+    if rec is None:
+        return None
+    h = hashlib.sha256()
+    for src in rec["sources"]:
+        with open(os.path.join(ROOT, "nvfp4_quantized_moe_token_gb300", src), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest()[:16] != rec["source_sha256_16"]:
+        return None
+    return rec["dram_read_bytes"] + rec["dram_write_bytes"]
+
+
 def algorithmic(R):
     """Per-launch algorithmic work of each stage (bytes or flops)."""
     b16, f32 = 2, 4
@@ -188,7 +222,7 @@ def run_ours(args, rank, world, local):
     need = nv.lib().moe_expert_workspace(T, H, F, E, K_TOP)
     ws = torch.zeros(need, dtype=torch.uint8, device=dev)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
     R = T * K_TOP
 
@@ -212,7 +246,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     torch.cuda.nvtx.range_push("timed")
     for i in range(args.steps):
-        flush.zero_()
+        flush()
         step(events[i])
     torch.cuda.synchronize()
     torch.cuda.nvtx.range_pop()
@@ -244,7 +278,7 @@ def run_ours(args, rank, world, local):
                  for _ in range(args.steps)]
         barrier(world)
         for a, b in pairs:
-            flush.zero_()
+            flush()
             a.record(stream)
             e2e_step()
             b.record(stream)
@@ -275,7 +309,7 @@ def run_ours(args, rank, world, local):
     dom = max(stages, key=lambda s: stages[s]["ms"])
     dm = stages[dom]
     roofline = {"kernel": dom, "bound": dm["bound"], "achieved": dm["achieved"], "peak": dm["peak"],
-                "unit": dm["unit"], "frac": dm["frac"], "traffic": None,
+                "unit": dm["unit"], "frac": dm["frac"], "traffic": recorded_traffic(dom),
                 "peak_source": f"{peak_src} ({'bf16 burst x 6 nominal FP4:BF16' if dm['bound'] == 'tensor' else 'copy GB/s'})",
                 "work_per_launch": alg[dom][1]}
 
@@ -298,14 +332,14 @@ def quant_gbs(args, local, reps=50):
     xb = workloads.quant_rows()["x"]
     x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).to(dev)
     q = nv.NVFP4Tensor.empty(16384, 2048, 16384, dev)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     for _ in range(5):
         nv.quantize_rows(x, out=q)
     ts = []
     torch.cuda.synchronize()
     torch.cuda.nvtx.range_push("timed_quant")
     for _ in range(reps):
-        flush.zero_()
+        flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         nv.quantize_rows(x, out=q)
@@ -315,8 +349,15 @@ def quant_gbs(args, local, reps=50):
     torch.cuda.nvtx.range_pop()
     ms = statistics.fmean(a.elapsed_time(b) for a, b in ts)
     nbytes = 16384 * (2048 * 2 + 1024 + 128 + 4)
-    return {"workload": "quantize 16384 x 2048", "us": ms * 1e3, "gbs": nbytes / (ms / 1e3) / 1e9,
-            "algorithmic_bytes": nbytes}
+    peaks = {}
+    pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk):
+        with open(pk) as f:
+            peaks = json.load(f)
+    hbm = peaks.get("hbm_gbs", 6800.0)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"workload": "quantize 16384 x 2048", "us": ms * 1e3, "gbs": gbs, "algorithmic_bytes": nbytes,
+            "frac_of_hbm": gbs / hbm, "hbm_peak_gbs": hbm, "traffic": recorded_traffic("quant")}
 
 
 # ---------------------------------------------------------------- oracle timing
