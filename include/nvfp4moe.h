@@ -236,6 +236,32 @@ NVFP4_API int moe_expert_forward(const void* x_bf16, int64_t T, int64_t H,
                        const moe_options* opt, void* out_bf16, const moe_debug* dbg,
                        void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * moe_expert_forward_noalloc: moe_expert_forward for callers that must not
+ * allocate device memory -- for example a plugin that its host framework
+ * hands only input and output buffers, or a latency-critical step in which
+ * cudaMalloc / cudaFree would synchronize the device.  The pages describe no
+ * such call; it is a deployment convenience of this library.
+ *   Arguments, layouts and results are those of moe_expert_forward (no
+ *   debug outputs).  The workspace is a fixed 32 MiB array in device global
+ *   memory inside the library, which every GPU that loads the library holds
+ *   until the process exits.  Sizes whose workspace
+ *   (moe_expert_workspace()) exceeds 32 MiB are rejected with
+ *   NVFP4_EWORKSPACE and a message; at hidden 2048, FFN 768, 128 experts,
+ *   top-8 that is more than 512 tokens.
+ *   The first call on each device looks the array's device address up
+ *   (cudaGetSymbolAddress) with that device current, so make it before any
+ *   stream capture.  Nothing is allocated, by this call or later ones.
+ *   All calls on a device share the one array: calls whose work overlaps on
+ *   the GPU (different streams without ordering) race and corrupt each
+ *   other.  Each call clears the device error word at the start of the
+ *   array; device-side error bits are not reported to the caller.
+ */
+NVFP4_API int moe_expert_forward_noalloc(const void* x_bf16, int64_t T, int64_t H,
+                                         const float* router_logits, const float* router_bias, int E,
+                                         int topk, const nvfp4_tensor* w1, const nvfp4_tensor* w2,
+                                         int64_t F, const moe_options* opt, void* out_bf16, void* stream);
+
 /* Message describing the last error returned on the calling thread ("" if none). */
 NVFP4_API const char* nvfp4_last_error(void);
 

@@ -48,7 +48,7 @@ PER_ROW = 0
 PER_TENSOR = 1
 SYMBOLS = ["nvfp4_sf_bytes", "nvfp4_quantize_workspace", "nvfp4_quantize_rows", "nvfp4_linear",
            "moe_expert_workspace_layout", "moe_expert_workspace", "moe_expert_forward",
-           "nvfp4_last_error"]
+           "moe_expert_forward_noalloc", "nvfp4_last_error"]
 
 
 class NVFP4Error(RuntimeError):

@@ -54,6 +54,11 @@ int check_tensor(const nvfp4_tensor* t, const char* name) {
 
 }  // namespace
 
+namespace nvfp4 {
+// Record a message for nvfp4_last_error() from another translation unit.
+int set_last_error(int code, const char* msg) { return fail(code, "%s", msg); }
+}  // namespace nvfp4
+
 extern "C" {
 
 const char* nvfp4_last_error(void) { return g_last_error.c_str(); }

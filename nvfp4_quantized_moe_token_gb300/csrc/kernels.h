@@ -92,5 +92,6 @@ struct CombineLaunch {
 cudaError_t launch_combine(const CombineLaunch& c, cudaStream_t stream);
 
 int device_sm_count();
+int set_last_error(int code, const char* msg);
 
 }  // namespace nvfp4

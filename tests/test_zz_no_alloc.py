@@ -1,0 +1,73 @@
+"""moe_expert_forward_noalloc: the expert layer for callers that must not
+allocate device memory (a plugin given only its input and output buffers,
+or a step where cudaMalloc would synchronize the device).  Its workspace is
+a fixed array inside the library, so the checks here are that it gives the
+same output as moe_expert_forward with a caller workspace, twice in a row on
+different inputs (the array keeps the previous call's contents), and that it
+refuses layers too large for the array.  Named to be collected last."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_quantized_moe_token_gb300 as nv
+import oracle
+import workloads
+from tests.helpers import bf16_bits, to_dev_bf16
+
+T, E, K, H, F = 200, 128, 8, 2048, 768  # about 14 MiB of workspace, inside the 32 MiB array
+
+
+def _lib():
+    L = nv.lib()
+    f = L.moe_expert_forward_noalloc
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                  ctypes.c_int, ctypes.c_int, ctypes.POINTER(nv._Tensor), ctypes.POINTER(nv._Tensor),
+                  ctypes.c_int64, ctypes.POINTER(nv._Options), ctypes.c_void_p, ctypes.c_void_p]
+    return L
+
+
+def _noalloc(L, x, logits, bias, w1q, w2q, out):
+    a, b = w1q.c(), w2q.c()
+    opt = nv._Options(0)
+    rc = L.moe_expert_forward_noalloc(x.data_ptr(), T, H, logits.data_ptr(), bias.data_ptr(), E, K,
+                                      ctypes.byref(a), ctypes.byref(b), F, ctypes.byref(opt), out.data_ptr(),
+                                      ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == 0, L.nvfp4_last_error().decode()
+
+
+@pytest.mark.gpu
+def test_noalloc_matches_workspace_call_on_two_calls_in_a_row():
+    L = _lib()
+    rng = np.random.default_rng(17)
+    w1 = workloads.gaussian_bf16(rng, (E, 2 * F, H), std=0.02)
+    w2 = workloads.gaussian_bf16(rng, (E, H, F), std=0.02)
+    w1q = nv.quantize_grouped_weights(to_dev_bf16(w1))
+    w2q = nv.quantize_grouped_weights(to_dev_bf16(w2))
+    for call in range(2):  # different inputs each call: nothing stale may leak through the shared array
+        x = to_dev_bf16(workloads.gaussian_bf16(rng, (T, H)))
+        logits = torch.from_numpy(rng.standard_normal((T, E), dtype=np.float32)).cuda()
+        bias = torch.from_numpy(rng.standard_normal(E, dtype=np.float32) * np.float32(2.0)).cuda()
+        ref, _ = nv.moe_expert_forward(x, logits, bias, w1q, w2q, F, K)
+        out = torch.full((T, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+        _noalloc(L, x, logits, bias, w1q, w2q, out)
+        torch.cuda.synchronize()
+        g = oracle.bf16_to_f64(bf16_bits(out))
+        r = oracle.bf16_to_f64(bf16_bits(ref))
+        assert np.all(np.isfinite(g)), f"call {call}: output not written"
+        # the tolerance of the combine parity tests: one bf16 ulp (same kernels, so in fact bitwise)
+        assert np.all(np.abs(g - r) <= oracle.bf16_ulp(np.maximum(np.abs(g), np.abs(r)))), f"call {call}"
+
+
+def test_noalloc_rejects_layers_beyond_the_array():
+    """Refused on the host before any CUDA call (runs without a GPU)."""
+    L = _lib()
+    w1 = nv._Tensor(4096, 4096, 4096, E * 2 * F, H)
+    w2 = nv._Tensor(4096, 4096, 4096, E * H, F)
+    opt = nv._Options(0)
+    rc = L.moe_expert_forward_noalloc(4096, 32768, H, 4096, None, E, K, ctypes.byref(w1), ctypes.byref(w2), F,
+                                      ctypes.byref(opt), 4096, None)
+    assert rc == -4
+    assert "scratch" in L.nvfp4_last_error().decode()
