@@ -121,6 +121,59 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
     }
 }
 
+// ---------------------------------------------------------------- clusters
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+// Arrive on an mbarrier given by its cluster address (possibly in the peer
+// CTA), with the instruction's default semantics.  Callers order their
+// tcgen05 stores and loads before it with tcgen05.wait + fence; a
+// .release.cluster arrive would also wait for every earlier memory access of
+// the thread to reach cluster scope, which costs several hundred cycles per
+// arrive under load.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" :: "r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+// As mbar_wait_bounded, acquiring at cluster scope (arrivals from the peer CTA).
+__device__ __forceinline__ bool mbar_wait_bounded_cluster(uint32_t bar, uint32_t parity,
+                                                          volatile int* abort, uint32_t* err) {
+    uint64_t start = 0;
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((i & 63u) == 63u) {
+            if (*abort) return false;
+            uint64_t now = globaltimer_ns();
+            if (start == 0) {
+                start = now;
+            } else if (now - start > kTimeoutNs) {
+                *abort = 1;
+                if (err) atomicOr(err, NVFP4_DEVERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- bulk copies (TMA)
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint32_t bar,
@@ -153,6 +206,40 @@ __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
 }
 
 // ---------------------------------------------------------------- tcgen05
+
+// CTA-pair forms (.cta_group::2): the allocation is made by one warp in each
+// CTA of the pair, the MMA is issued by one thread of the even CTA and
+// writes both CTAs' TMEM, commits can arrive on both CTAs' barriers.
+__device__ __forceinline__ void tmem_alloc2(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(dst_smem), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish2() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols) : "memory");
+}
+// Arrive on the mbarrier at this shared-memory offset in every CTA of `mask`
+// once all tcgen05 operations issued so far by this thread have completed.
+__device__ __forceinline__ void tc_commit2_mc(uint32_t bar, uint16_t mask) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+                 :: "r"(bar), "h"(mask) : "memory");
+}
+// D[tmem of both CTAs] (+)= A[smem, M/2 rows in each CTA] x B[smem, N/2 rows
+// in each CTA]^T, NVFP4 block-scaled, M = 256 across the pair.
+__device__ __forceinline__ void tc_mma2_nvfp4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
+        " [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
+           "r"(accumulate)
+        : "memory");
+}
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"

@@ -7,34 +7,46 @@
 // x alpha_b; C = gate | up; D = act(gate, up) (x prob); amax of D reduced
 // concurrently across CTAs).
 //
-// Persistent kernel, one CTA per SM, 22 warps with fixed roles:
-//   warp 0       TMA producer: per K-stage the A tile (128 rows x 128 FP4,
-//                64B-swizzled), the B tile (256 rows: two 128-row boxes) and
-//                the E4M3 scale atoms of both (plain bulk copies: the
-//                quantizer wrote them in the MMA's layout), 6-stage ring.
-//   warp 1       TMEM allocator and MMA issuer: per stage two
-//                tcgen05.mma.kind::mxf4nvf4.block_scale (M=128, N=256,
-//                K=64), fp32 accumulation in TMEM; tcgen05.commit frees the
-//                smem stage and, after the last stage, hands the accumulator
-//                to the epilogue.
+// Persistent kernel over CTA pairs (clusters of 2, one CTA per SM).  A pair
+// computes a 256 x 256 output tile with tcgen05.mma.cta_group::2: each CTA
+// stages its own 128 rows of A and one 128-row half of the 256 weight rows,
+// the tensor cores of both SMs read both halves of B, and each CTA's TMEM
+// receives its own 128 rows of the accumulator.  Per SM that halves the
+// weight bytes moved per tile (the single-CTA M=128 x N=256 form is limited
+// by the bytes it must stage, not by the tensor pipe), and one MMA issue
+// does the work of two.  Roles, 22 warps per CTA:
+//   warp 0       TMA producer (both CTAs): per K-stage its A tile (128 rows),
+//                its B half (128 rows) and the E4M3 scale atoms (plain bulk
+//                copies: the quantizer wrote them in the MMA's layout); the
+//                weight scales of both halves, since each SM's tensor core
+//                applies the scales of all 256 columns.
+//   warp 1       TMEM allocation (pair-collective, 512 columns) and, in the
+//                even CTA only, the MMA issuer: per stage tcgen05.mma
+//                .cta_group::2.kind::mxf4nvf4.block_scale (M=256, N=256,
+//                K=64), fp32 accumulation; tcgen05.commit multicast to both
+//                CTAs frees their smem stages and, after the last stage,
+//                hands both accumulator halves to the epilogues.
 //   warps 2-5    scale writers (one per TMEM lane quarter): move each stage's
-//                scale atoms from shared memory into TMEM with tcgen05.st.
+//                scale atoms from shared memory into the CTA's TMEM with
+//                tcgen05.st, then arrive on the even CTA's barrier.
 //                (tcgen05.cp would do the same copy, but every cp instruction
-//                occupies the tensor pipe for ~55-80 cycles whatever its size,
-//                three of them per MMA; tcgen05.st runs on the warps.)
+//                occupies the tensor pipe for ~55-80 cycles whatever its size;
+//                tcgen05.st runs on the warps.)
 //   warps 6-21   epilogue: each warp copies its 32 rows x 64 accumulator
-//                columns into registers, releases TMEM at once (the next
-//                tile's MMAs start), then scales and either converts to bf16
-//                (mode 0) or computes SwiGLU -> bf16 D + row amax (mode 1).
-//                Outputs leave through a per-warp shared-memory box of 32
-//                rows x 32 columns and a TMA tensor store (coalesced, off the
-//                warps); a warp whose 32 rows straddle the end of an expert
-//                group stores its valid rows directly instead.
-// Tiles are ordered (padded m-tile, n-tile) with n fastest, so CTAs running
-// at the same time share the A rows and one expert's weights in L2.
-// Every pipeline wait is bounded in time; a wait that runs out raises an
-// abort flag, records NVFP4_DEVERR_TIMEOUT, drains what is in flight and
-// lets the CTA exit normally (TMEM freed).
+//                columns into registers, releases TMEM at once (arriving on
+//                the even CTA's barrier: the next tile's MMAs start), then
+//                scales and either converts to bf16 (mode 0) or computes
+//                SwiGLU -> bf16 D + row amax (mode 1).  Mode 0 outputs leave
+//                through a per-warp shared-memory box of 32 rows x 32 columns
+//                and a TMA tensor store; a warp whose 32 rows straddle the end
+//                of an expert group stores its valid rows directly.
+// Work units are (pair of m-tiles of one group, n-tile), n fastest, so pairs
+// running at the same time share the A rows and one expert's weights in L2.
+// A group with an odd number of m-tiles ends in a unit whose odd CTA has no
+// rows: it repeats its partner's A rows for the MMA and stores nothing.
+// Every pipeline wait is bounded in time; a wait that runs out raises the
+// abort flag of both CTAs, records NVFP4_DEVERR_TIMEOUT, drains what is in
+// flight and lets both CTAs exit normally (TMEM freed).
 #include <cuda.h>
 
 #include <mutex>
@@ -46,7 +58,7 @@ namespace nvfp4 {
 
 namespace {
 
-constexpr int BM = 128;                 // rows per tile (TMEM lanes)
+constexpr int BM = 128;                 // rows per CTA (TMEM lanes); a pair covers 2 * BM
 constexpr int BN = 256;                 // accumulator columns per tile
 constexpr int EPI_WARP0 = 6;            // warps 2..5 write scales, 6..21 run the epilogue
 constexpr int EPI_WARPS = 16;
@@ -55,30 +67,31 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;
 constexpr uint32_t SF_COL = 256;
 constexpr int MAX_G = 256;
-constexpr uint32_t IDESC = idesc_nvfp4(BM, BN);
+constexpr uint32_t IDESC = idesc_nvfp4(2 * BM, BN);
 constexpr int STG_BYTES = 32 * 64;      // per-warp output staging box: 32 rows x 32 bf16
 
 // Pipeline shape per epilogue mode.  The plain (mode 0) epilogue writes a
-// full 128 x 256 bf16 tile per K loop of at most a few stages (FC2: K = 768),
-// so it takes 64-byte K-stages (6 in flight) and leaves room for the TMA-store
-// staging boxes.  The SwiGLU (mode 1) epilogue writes half as much per much
-// longer K loop (FC1: K = 2048): it keeps 128-byte K-stages (4 in flight,
-// more bytes per TMA request) and stores directly.
+// full 128 x 256 bf16 tile per CTA per K loop of a few stages (FC2: K = 768),
+// so it takes 64-byte K-stages (8 in flight) and leaves room for the
+// TMA-store staging boxes.  The SwiGLU (mode 1) epilogue writes half as much
+// per much longer K loop (FC1: K = 2048): 128-byte K-stages (5 in flight,
+// more bytes per TMA request), direct stores.
 template <int MODE>
 struct Cfg {
     static constexpr int BK = MODE == 0 ? 128 : 256;    // FP4 elements of K per stage
     static constexpr int ROWB = BK / 2;                 // bytes per row per stage
-    static constexpr int STAGES = MODE == 0 ? 6 : 4;
-    static constexpr int A_BYTES = BM * ROWB;
-    static constexpr int B_BYTES = BN * ROWB;
+    static constexpr int STAGES = MODE == 0 ? 8 : 5;
+    static constexpr int A_BYTES = BM * ROWB;           // this CTA's 128 rows of A
+    static constexpr int B_BYTES = 128 * ROWB;          // this CTA's half of the 256 weight rows
     static constexpr int ATOMS = BK / 64;               // scale atoms per 128 rows per stage
     static constexpr int SFA_BYTES = ATOMS * 512;
-    static constexpr int SFB_BYTES = 2 * ATOMS * 512;
+    static constexpr int SFB_BYTES = 2 * ATOMS * 512;   // weight scales of both halves
     static constexpr int SWZ = MODE == 0 ? 4 : 2;       // descriptor swizzle code: 64B / 128B
     static constexpr int SBO = 8 * ROWB;                // bytes between 8-row core-matrix groups
     static constexpr uint32_t SF_STAGE_COLS = 12 * ATOMS;  // SFA 4*ATOMS + SFB 8*ATOMS columns
     static constexpr bool STAGED = MODE == 0;
     static constexpr int NSTG = STAGED ? EPI_WARPS : 0;
+    static_assert(SF_COL + STAGES * SF_STAGE_COLS <= TMEM_COLS, "scale columns exceed TMEM");
 };
 
 template <int MODE>
@@ -89,17 +102,17 @@ struct __align__(1024) Smem {
     uint8_t sfa[C::STAGES][C::SFA_BYTES];
     uint8_t sfb[C::STAGES][C::SFB_BYTES];
     uint8_t stg[C::NSTG > 0 ? C::NSTG : 1][C::NSTG > 0 ? STG_BYTES : 16];
-    uint64_t full[C::STAGES];      // TMA bytes landed
-    uint64_t sf_full[C::STAGES];   // scales of the stage written to TMEM (4 warps)
-    uint64_t empty[C::STAGES];     // MMAs of the stage done (commit)
-    uint64_t tmem_full;
-    uint64_t tmem_empty;
+    uint64_t full[C::STAGES];      // this CTA's TMA bytes landed
+    uint64_t sf_full[C::STAGES];   // (even CTA) scales of the stage in TMEM: 4 warps of each CTA
+    uint64_t empty[C::STAGES];     // MMAs of the stage done (commit, multicast to the pair)
+    uint64_t tmem_full;            // accumulator ready (commit, multicast to the pair)
+    uint64_t tmem_empty;           // (even CTA) accumulator drained: 16 warps of each CTA
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
-    int consumed;               // stages the MMA issuer has taken from the ring
     int goff[MAX_G + 1];
     int gpoff[MAX_G + 1];
+    int ppre[MAX_G + 1];           // units of m-tile pairs before each group
 };
 
 struct KParams {
@@ -124,22 +137,36 @@ struct Tile {
     int g, row0, rows, mt, nt;
 };
 
+// Unit u = (pair row pr, n-tile nt), nt fastest.  Pair row pr lies in the
+// group g with ppre[g] <= pr < ppre[g + 1]; CTA `rank` of the pair takes
+// m-tile gpoff[g] / BM + 2 (pr - ppre[g]) + rank.  Past the group's last
+// m-tile that CTA has no rows (rows = 0) and repeats its partner's m-tile.
 template <class S>
-__device__ __forceinline__ Tile decode_tile(const S& s, int G, int n_tiles, int t) {
+__device__ __forceinline__ Tile decode_unit(const S& s, int G, int n_tiles, int u, uint32_t rank) {
     Tile x;
-    x.mt = t / n_tiles;
-    x.nt = t - x.mt * n_tiles;
-    const int prow = x.mt * BM;
-    int lo = 0, hi = G;  // last g with gpoff[g] <= prow (non-empty groups are unique)
+    const int pr = u / n_tiles;
+    x.nt = u - pr * n_tiles;
+    int lo = 0, hi = G;  // last g with ppre[g] <= pr (the group holding pair row pr)
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (s.gpoff[mid] <= prow) lo = mid; else hi = mid;
+        if (s.ppre[mid] <= pr) lo = mid; else hi = mid;
     }
     x.g = lo;
-    x.row0 = s.goff[lo] + (prow - s.gpoff[lo]);
+    const int mt0 = s.gpoff[lo] / BM + 2 * (pr - s.ppre[lo]);
+    const bool none = mt0 + (int)rank >= s.gpoff[lo + 1] / BM;
+    x.mt = none ? mt0 : mt0 + (int)rank;
+    x.row0 = s.goff[lo] + (x.mt * BM - s.gpoff[lo]);
     const int end = s.goff[lo + 1];
-    x.rows = end - x.row0 < BM ? end - x.row0 : BM;
+    x.rows = none ? 0 : (end - x.row0 < BM ? end - x.row0 : BM);
     return x;
+}
+
+// Set the abort flag of both CTAs of the pair (the peer's through its
+// shared-memory window), so its bounded waits give up at once.
+__device__ __forceinline__ void raise_abort(int* abort_flag, uint32_t rank) {
+    *(volatile int*)abort_flag = 1;
+    const uint32_t peer = mapa_shared(smem_u32(abort_flag), rank ^ 1u);
+    asm volatile("st.relaxed.cluster.shared::cluster.u32 [%0], %1;" :: "r"(peer), "r"(1) : "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -185,7 +212,7 @@ __device__ __forceinline__ float silu(float g) {
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ CUtensorMap tmO, const KParams p) {
     using C = Cfg<MODE>;
@@ -196,6 +223,8 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     Smem<MODE>& s = *reinterpret_cast<Smem<MODE>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.G;
+    const uint32_t rank = cluster_ctarank();
+    const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
 
     // group table: dense calls are one group of M rows
     if (p.goff == nullptr) {
@@ -209,26 +238,49 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
             mbar_init(smem_u32(&s.full[i]), 1);
-            mbar_init(smem_u32(&s.sf_full[i]), 4);
+            mbar_init(smem_u32(&s.sf_full[i]), 8);
             mbar_init(smem_u32(&s.empty[i]), 1);
         }
         mbar_init(smem_u32(&s.tmem_full), 1);
-        mbar_init(smem_u32(&s.tmem_empty), EPI_WARPS);
+        mbar_init(smem_u32(&s.tmem_empty), 2 * EPI_WARPS);
         mbar_init(smem_u32(&s.drain), 1);
         s.abort = 0;
-        s.consumed = 0;
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) { prefetch_tmap(&tmA); prefetch_tmap(&tmB); prefetch_tmap(&tmO); }
-    if (warp == 1) { tmem_alloc(smem_u32(&s.tmem_base), TMEM_COLS); tmem_relinquish(); }
-    tc_fence_before();
+    if (warp == 1) { tmem_alloc2(smem_u32(&s.tmem_base), TMEM_COLS); tmem_relinquish2(); }
     __syncthreads();
+    if (warp == 0) {
+        // ppre[g] = sum over groups before g of ceil(m-tiles / 2); lane l holds groups 8l..8l+7
+        int loc[8], sum = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int g = lane * 8 + j;
+            loc[j] = sum;
+            sum += g < G ? ((s.gpoff[g + 1] - s.gpoff[g]) / BM + 1) >> 1 : 0;
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int g = lane * 8 + j;
+            if (g < G) s.ppre[g] = incl - sum + loc[j];
+        }
+        if (lane == 31) s.ppre[G] = incl;
+    }
+    // barriers initialised and TMEM allocated in both CTAs before any remote arrival
+    tc_fence_before();
+    cluster_sync();
     tc_fence_after();
     const uint32_t tmem = s.tmem_base;
     volatile int* abort = &s.abort;
 
     const int n_tiles = MODE == 1 ? p.N / 256 : p.N / BN;  // mode 1: 128 gate + 128 up columns per tile
-    const int total = (s.gpoff[G] / BM) * n_tiles;
+    const int total = s.ppre[G] * n_tiles;
     const int k_atoms = p.K / 64;
     const int k_stages = (k_atoms + ATOMS - 1) / ATOMS;
 
@@ -237,72 +289,67 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             // ------------------------------------------------------------ producer
             int stage = 0;
             uint32_t phase = 0;
-            int issued = 0;
             int last_phase[STAGES];
             for (int i = 0; i < STAGES; ++i) last_phase[i] = -1;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const Tile x = decode_tile(s, G, n_tiles, t);
+            for (int u = pair; u < total && ok; u += n_pairs) {
+                const Tile x = decode_unit(s, G, n_tiles, u, rank);
                 const int jb0 = MODE == 1 ? x.g * (p.N / 128) + x.nt : x.g * (p.N / 128) + 2 * x.nt;
                 const int jb1 = MODE == 1 ? x.g * (p.N / 128) + p.N / 256 + x.nt : jb0 + 1;
+                const int jb = rank == 0 ? jb0 : jb1;
                 for (int ks = 0; ks < k_stages; ++ks) {
                     if (!mbar_wait_bounded(smem_u32(&s.empty[stage]), phase ^ 1, abort, p.err)) { ok = false; break; }
                     const int na = k_atoms - ks * ATOMS < ATOMS ? k_atoms - ks * ATOMS : ATOMS;
                     const uint32_t fb = smem_u32(&s.full[stage]);
                     mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES + 3 * na * 512);
                     tma_load_2d(smem_u32(s.a[stage]), &tmA, fb, ks * ROWB, x.row0);
-                    tma_load_2d(smem_u32(s.b[stage]), &tmB, fb, ks * ROWB, jb0 * 128);
-                    tma_load_2d(smem_u32(s.b[stage]) + B_BYTES / 2, &tmB, fb, ks * ROWB, jb1 * 128);
+                    tma_load_2d(smem_u32(s.b[stage]), &tmB, fb, ks * ROWB, jb * 128);
                     bulk_load(smem_u32(s.sfa[stage]), p.a_sf + ((int64_t)x.mt * k_atoms + ks * ATOMS) * 512, na * 512, fb);
                     bulk_load(smem_u32(s.sfb[stage]), p.b_sf + ((int64_t)jb0 * k_atoms + ks * ATOMS) * 512, na * 512, fb);
                     bulk_load(smem_u32(s.sfb[stage]) + SFB_BYTES / 2,
                               p.b_sf + ((int64_t)jb1 * k_atoms + ks * ATOMS) * 512, na * 512, fb);
                     last_phase[stage] = (int)phase;
-                    ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
             }
             if (!ok) {
-                // drain: wait (bounded) for loads the MMA issuer never consumed
-                const int outstanding = issued - *(volatile int*)&s.consumed;
-                int st = stage;
-                for (int i = 0; i < outstanding && i < STAGES; ++i) {
-                    st = st == 0 ? STAGES - 1 : st - 1;
+                raise_abort(&s.abort, rank);
+                // drain: the last load issued into each stage has landed (bounded wait)
+                for (int st = 0; st < STAGES; ++st)
                     if (last_phase[st] >= 0) mbar_wait_drain(smem_u32(&s.full[st]), (uint32_t)last_phase[st]);
-                }
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && rank == 0) {
+            // ------------------------------------------------------------ MMA issuer (even CTA)
             int stage = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                if (!mbar_wait_bounded(smem_u32(&s.tmem_empty), acc_phase ^ 1, abort, p.err)) { ok = false; break; }
+            for (int u = pair; u < total && ok; u += n_pairs) {
+                if (!mbar_wait_bounded_cluster(smem_u32(&s.tmem_empty), acc_phase ^ 1, abort, p.err)) { ok = false; break; }
                 tc_fence_after();
                 for (int ks = 0; ks < k_stages; ++ks) {
                     if (!mbar_wait_bounded(smem_u32(&s.full[stage]), phase, abort, p.err) ||
-                        !mbar_wait_bounded(smem_u32(&s.sf_full[stage]), phase, abort, p.err)) { ok = false; break; }
-                    *(volatile int*)&s.consumed += 1;
+                        !mbar_wait_bounded_cluster(smem_u32(&s.sf_full[stage]), phase, abort, p.err)) { ok = false; break; }
                     tc_fence_after();
                     const int na = k_atoms - ks * ATOMS < ATOMS ? k_atoms - ks * ATOMS : ATOMS;
                     const uint32_t sfc = tmem + SF_COL + stage * SF_STAGE_COLS;
                     const uint32_t a0 = smem_u32(s.a[stage]), b0 = smem_u32(s.b[stage]);
                     for (int kk = 0; kk < na; ++kk) {
-                        tc_mma_nvfp4(tmem + ACC_COL, smem_desc(a0 + kk * 32, 0, SBO, SWZ),
-                                     smem_desc(b0 + kk * 32, 0, SBO, SWZ), IDESC,
-                                     sfc + kk * 4, sfc + 4 * ATOMS + kk * 8, (ks | kk) != 0);
+                        tc_mma2_nvfp4(tmem + ACC_COL, smem_desc(a0 + kk * 32, 0, SBO, SWZ),
+                                      smem_desc(b0 + kk * 32, 0, SBO, SWZ), IDESC,
+                                      sfc + kk * 4, sfc + 4 * ATOMS + kk * 8, (ks | kk) != 0);
                     }
-                    tc_commit(smem_u32(&s.empty[stage]));
+                    tc_commit2_mc(smem_u32(&s.empty[stage]), 3);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
-                tc_commit(smem_u32(&s.tmem_full));
+                tc_commit2_mc(smem_u32(&s.tmem_full), 3);
                 acc_phase ^= 1;
             }
+            if (!ok) raise_abort(&s.abort, rank);
             // every MMA issued by this thread completes before TMEM is released
-            tc_commit(smem_u32(&s.drain));
+            tc_commit2_mc(smem_u32(&s.drain), 1);
             mbar_wait_drain(smem_u32(&s.drain), 0);
         }
     } else if (warp < EPI_WARP0) {
@@ -317,7 +364,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        for (int u = pair; u < total && ok; u += n_pairs) {
             for (int ks = 0; ks < k_stages; ++ks) {
                 if (!mbar_wait_bounded(smem_u32(&s.full[stage]), phase, abort, p.err)) { ok = false; break; }
                 const uint32_t sfc = lane_addr + SF_COL + stage * SF_STAGE_COLS;
@@ -333,10 +380,11 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&s.sf_full[stage]));
+                if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&s.sf_full[stage]), 0));
                 if (++stage == STAGES) { stage = 0; phase ^= 1; }
             }
         }
+        if (!ok && lane == 0) raise_abort(&s.abort, rank);
     } else {
         // ---------------------------------------------------------------- epilogue
         // Each warp copies its 32 rows x 64 accumulator columns into registers
@@ -345,9 +393,11 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         const int q = warp & 3;                    // TMEM lane quarter this warp may access
         const int cg = (warp - EPI_WARP0) >> 2;    // column group 0..3
         const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
+        const uint32_t release = mapa_shared(smem_u32(&s.tmem_empty), 0);
         uint32_t acc_phase = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            const Tile x = decode_tile(s, G, n_tiles, t);
+        bool ok = true;
+        for (int u = pair; u < total; u += n_pairs) {
+            const Tile x = decode_unit(s, G, n_tiles, u, rank);
             const int rl = q * 32 + lane;
             const bool valid = rl < x.rows;
             const int64_t row = (int64_t)x.row0 + rl;
@@ -355,7 +405,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             const float sa = valid ? __ldg(p.a_scale + row) : 0.0f;
             const float sbw = __ldg(p.b_scale + x.g);
             const float prob = (valid && p.row_prob) ? __ldg(p.row_prob + row) : 1.0f;
-            if (!mbar_wait_bounded(smem_u32(&s.tmem_full), acc_phase, abort, p.err)) break;
+            if (!mbar_wait_bounded_cluster(smem_u32(&s.tmem_full), acc_phase, abort, p.err)) { ok = false; break; }
             tc_fence_after();
             uint32_t v[64];
             if (MODE == 0) {
@@ -368,8 +418,9 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&s.tmem_empty));
+            if (lane == 0) mbar_arrive_cluster(release);
             acc_phase ^= 1;
+            if (x.rows == 0) continue;  // the odd CTA of a group's last pair: nothing to store
             const float scale = __fmul_rn(sa, sbw);
             // all 32 rows of this warp inside the tile's group: TMA store; else direct
             const bool full_warp = q * 32 + 32 <= x.rows;
@@ -405,8 +456,8 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const float g = __uint_as_float(v[2 * j + e]) * scale;
-                        const float u = __uint_as_float(v[32 + 2 * j + e]) * scale;
-                        float dv = silu(g) * u;
+                        const float u2 = __uint_as_float(v[32 + 2 * j + e]) * scale;
+                        float dv = silu(g) * u2;
                         if (p.row_prob) dv *= prob;
                         m = fmaxf(m, fabsf(dv));
                         d2[e] = dv;
@@ -421,14 +472,17 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 }
             }
         }
+        if (!ok && lane == 0) raise_abort(&s.abort, rank);
         if (C::STAGED && lane == 0) bulk_wait_all();  // this warp's tensor stores are complete before exit
         __syncwarp();
     }
+    // neither CTA leaves while the pair's MMAs, commits or arrivals may still touch it
     tc_fence_before();
-    __syncthreads();
+    __syncwarp();
+    cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, TMEM_COLS);
+        tmem_dealloc2(tmem, TMEM_COLS);
     }
 }
 
@@ -480,6 +534,56 @@ bool make_out_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Pairs that can be resident at once for the kernel of one mode (clusters of
+// two CTAs of one SM each), from the occupancy calculator; 0 on failure.
+template <int MODE>
+int resident_pairs(size_t smem, int num_sms) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(num_sms & ~1), 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_nvfp4_kernel<MODE>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+template <int MODE>
+cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const KParams& p,
+                        int num_sms, int64_t dense_units, cudaStream_t stream) {
+    const size_t smem = sizeof(Smem<MODE>) + 1024;
+    static std::mutex mu;
+    static int pairs_cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    int pairs = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev >= 0 && dev < 64) pairs = pairs_cache[dev];
+        if (pairs == 0) {
+            cudaError_t e = cudaFuncSetAttribute(gemm_nvfp4_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)smem);
+            if (e != cudaSuccess) return e;
+            pairs = resident_pairs<MODE>(smem, num_sms);
+            if (pairs <= 0) pairs = num_sms / 2;
+            if (dev >= 0 && dev < 64) pairs_cache[dev] = pairs;
+        }
+    }
+    if (dense_units > 0 && dense_units < pairs) pairs = (int)dense_units;
+    if (pairs < 1) pairs = 1;
+    gemm_nvfp4_kernel<MODE><<<2 * pairs, THREADS, smem, stream>>>(ta, tb, to, p);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 int device_sm_count() {
@@ -517,31 +621,11 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
     p.row_prob = g.row_prob;
     p.c_debug = g.c_debug;
     p.err = g.err;
-    int grid = g.num_sms > 0 ? g.num_sms : 148;
-    if (g.goff == nullptr) {
-        const int64_t tiles = (g.M + BM - 1) / BM * (g.N / BN);
-        if (tiles < grid) grid = (int)tiles;
-    }
-    if (g.mode == 0) {
-        const size_t smem = sizeof(Smem<0>) + 1024;
-        static std::once_flag once0;
-        static cudaError_t err0 = cudaSuccess;
-        std::call_once(once0, [&] {
-            err0 = cudaFuncSetAttribute(gemm_nvfp4_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        });
-        if (err0 != cudaSuccess) return err0;
-        gemm_nvfp4_kernel<0><<<grid, THREADS, smem, stream>>>(ta, tb, to, p);
-    } else {
-        const size_t smem = sizeof(Smem<1>) + 1024;
-        static std::once_flag once1;
-        static cudaError_t err1 = cudaSuccess;
-        std::call_once(once1, [&] {
-            err1 = cudaFuncSetAttribute(gemm_nvfp4_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        });
-        if (err1 != cudaSuccess) return err1;
-        gemm_nvfp4_kernel<1><<<grid, THREADS, smem, stream>>>(ta, tb, to, p);
-    }
-    return cudaGetLastError();
+    const int num_sms = g.num_sms > 0 ? g.num_sms : 148;
+    // dense calls: no more pairs than units of work (m-tile pairs x n-tiles)
+    const int64_t dense_units = g.goff == nullptr ? ((g.M + BM - 1) / BM + 1) / 2 * (g.N / BN) : 0;
+    if (g.mode == 0) return launch_mode<0>(ta, tb, to, p, num_sms, dense_units, stream);
+    return launch_mode<1>(ta, tb, to, p, num_sms, dense_units, stream);
 }
 
 }  // namespace nvfp4
