@@ -185,7 +185,7 @@ typedef struct moe_workspace_layout {
     size_t inv;          /* int32 [T x topk] expert-ordered row of (t, slot) */
     size_t chunk_counts; /* int32 scratch for the stable scatter */
     size_t xq_codes;     /* uint8 [T x H/2] per-token quantized X */
-    size_t xq_sf;        /* swizzled [T x H/16] */
+    size_t xq_sf;        /* row-linear [T x H/16] (the permute reads whole rows) */
     size_t xq_scale;     /* fp32 [T] */
     size_t a1_codes;     /* uint8 [R x H/2] X rows in expert order */
     size_t a1_sf;        /* swizzled, expert e's rows start at padded row padded_offsets[e] */

@@ -241,7 +241,8 @@ int moe_expert_forward(const void* x_bf16, int64_t T, int64_t H, const float* ro
     };
     if ((e = mark()) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe event: %s", cudaGetErrorString(e));
 
-    // 1. per-token quantization of X (once per token; the permute moves the result)
+    // 1. per-token quantization of X (once per token; the permute moves the
+    //    result, scales row-linear here and swizzled in the permuted copy)
     nvfp4::QuantLaunch qx{};
     qx.x = x_bf16;
     qx.ld = H;
@@ -249,6 +250,7 @@ int moe_expert_forward(const void* x_bf16, int64_t T, int64_t H, const float* ro
     qx.cols = H;
     qx.codes = at(L.xq_codes);
     qx.sf = at(L.xq_sf);
+    qx.sf_ld = H / 16;  // row-linear: the permute gathers whole rows of scales
     qx.scale = reinterpret_cast<float*>(at(L.xq_scale));
     qx.err = reinterpret_cast<uint32_t*>(at(L.err));
     if ((e = nvfp4::launch_quantize(qx, s)) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe quantize: %s", cudaGetErrorString(e));

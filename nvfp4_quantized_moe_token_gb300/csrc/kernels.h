@@ -14,6 +14,7 @@ struct QuantLaunch {
     int per_tensor;
     uint8_t* codes;
     uint8_t* sf;
+    int64_t sf_ld;          // 0: swizzled MMA layout; > 0: row-linear, sf_ld bytes per row (multiple of 4)
     float* scale;
     const int* goff;        // nullable: scale rows remapped by group padding
     const int* gpoff;
@@ -69,7 +70,7 @@ struct RouteLaunch {
     uint32_t* err;
     // permute (gather quantized X rows into expert order)
     const uint8_t* xq_codes;
-    const uint8_t* xq_sf;
+    const uint8_t* xq_sf;  // row-linear [T x H/16]
     const float* xq_scale;
     int64_t H;
     uint8_t* a1_codes;

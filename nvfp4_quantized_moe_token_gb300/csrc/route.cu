@@ -165,34 +165,75 @@ __global__ void __launch_bounds__(kThreads) route_scatter_kernel(RouteLaunch p) 
     }
 }
 
-// Permute: one warp per expert-ordered row r copies the codes, the block
-// scales (into the 128-row-padded layout of its expert) and the outer scale
-// of token perm[r] / k.
-__global__ void __launch_bounds__(kThreads) route_permute_kernel(RouteLaunch p, int64_t R) {
-    __shared__ int soff[257], spoff[257];
+// Permute: one CTA per 128-row padded m-tile of an expert.  Rows of the tile
+// are the expert-ordered rows pos0 .. pos0 + 127 (fewer in the expert's last
+// tile); row i copies the codes, the block scales and the outer scale of
+// token perm[pos0 + i] / k.  The codes move row by row (1 KB per row at
+// H = 2048, four rows in flight per warp).  The scales of the tile are
+// gathered from the row-linear X scales (one coalesced 4-byte word per lane
+// per row) into shared memory, then leave as the tile's contiguous run of
+// swizzled 512-byte atoms, so every global store is a whole 16-byte line;
+// rows past the expert's end get zero scales.
+constexpr int kTileRows = 128;
+
+__global__ void __launch_bounds__(kThreads) route_permute_kernel(RouteLaunch p) {
+    __shared__ uint32_t ssf[kTileRows][33];  // [row][scale group], stride 33 words: no bank conflicts
+    __shared__ int stok[kTileRows];
     const int E = p.E;
-    for (int i = threadIdx.x; i <= E; i += kThreads) { soff[i] = __ldg(p.off + i); spoff[i] = __ldg(p.poff + i); }
-    __syncthreads();
-    const int lane = threadIdx.x & 31;
-    const int64_t r = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
-    if (r >= R) return;
-    int lo = 0, hi = E;  // expert e with off[e] <= r < off[e+1]
+    const int prow0 = blockIdx.x * kTileRows;
+    if (prow0 >= __ldg(p.poff + E)) return;
+    int lo = 0, hi = E;  // the expert whose padded rows hold prow0
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (soff[mid] <= r) lo = mid; else hi = mid;
+        if (__ldg(p.poff + mid) <= prow0) lo = mid; else hi = mid;
     }
-    const int64_t prow = spoff[lo] + (r - soff[lo]);
-    const int64_t t = __ldg(p.perm + r) / p.k;
+    const int pos0 = __ldg(p.off + lo) + (prow0 - __ldg(p.poff + lo));
+    const int end = __ldg(p.off + lo + 1);
+    const int nrows = end - pos0 < kTileRows ? end - pos0 : kTileRows;
+    for (int i = threadIdx.x; i < kTileRows; i += kThreads) stok[i] = i < nrows ? __ldg(p.perm + pos0 + i) / p.k : -1;
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int W = kThreads / 32;
+
+    // codes: warp w copies rows w, w + W, ..., four rows per batch
     const int64_t row_bytes = p.H / 2;
-    const uint8_t* src = p.xq_codes + t * row_bytes;
-    uint8_t* dst = p.a1_codes + r * row_bytes;
-    for (int64_t c = lane * 16; c < row_bytes; c += 512)
-        *reinterpret_cast<uint4*>(dst + c) = __ldg(reinterpret_cast<const uint4*>(src + c));
+    for (int i0 = warp; i0 < nrows; i0 += 4 * W) {
+        for (int64_t c = lane * 16; c < row_bytes; c += 512) {
+            uint4 v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int i = i0 + j * W;
+                if (i < nrows) v[j] = __ldg(reinterpret_cast<const uint4*>(p.xq_codes + stok[i] * row_bytes + c));
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int i = i0 + j * W;
+                if (i < nrows) *reinterpret_cast<uint4*>(p.a1_codes + (int64_t)(pos0 + i) * row_bytes + c) = v[j];
+            }
+        }
+    }
+    for (int i = threadIdx.x; i < nrows; i += kThreads) p.a1_scale[pos0 + i] = __ldg(p.xq_scale + stok[i]);
+
+    // block scales, 32 groups of 4 (128 columns of scales) per pass
     const int64_t sp4 = p.H / 64;
-    for (int64_t q = lane; q < sp4; q += 32)
-        *reinterpret_cast<uint32_t*>(p.a1_sf + sf_group_offset(prow, q, sp4)) =
-            __ldg(reinterpret_cast<const uint32_t*>(p.xq_sf + sf_group_offset(t, q, sp4)));
-    if (lane == 0) p.a1_scale[r] = __ldg(p.xq_scale + t);
+    const int64_t sf_ld = p.H / 16;
+    uint8_t* tile_sf = p.a1_sf + (int64_t)blockIdx.x * sp4 * 512;
+    for (int64_t q0 = 0; q0 < sp4; q0 += 32) {
+        const int nq = sp4 - q0 < 32 ? (int)(sp4 - q0) : 32;
+        for (int i = warp; i < kTileRows; i += W) {
+            const int t = stok[i];
+            ssf[i][lane] = (t >= 0 && lane < nq)
+                ? __ldg(reinterpret_cast<const uint32_t*>(p.xq_sf + (int64_t)t * sf_ld + (q0 + lane) * 4)) : 0u;
+        }
+        __syncthreads();
+        // line c of the pass: group q0 + c / 32, line l = c % 32 holds rows l, l+32, l+64, l+96
+        for (int c = threadIdx.x; c < nq * 32; c += kThreads) {
+            const int q = c >> 5, l = c & 31;
+            *reinterpret_cast<uint4*>(tile_sf + (q0 + q) * 512 + l * 16) =
+                make_uint4(ssf[l][q], ssf[l + 32][q], ssf[l + 64][q], ssf[l + 96][q]);
+        }
+        __syncthreads();
+    }
 }
 
 }  // namespace
@@ -218,8 +259,9 @@ cudaError_t launch_route(const RouteLaunch& r, cudaStream_t stream) {
     route_scatter_kernel<<<nchunks, kThreads, sizeof(uint32_t) * r.E, stream>>>(r);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    // padded m-tiles: sum over experts of ceil(count / 128) <= R / 128 + E; CTAs past the last tile exit
     const int64_t R = r.T * r.k;
-    route_permute_kernel<<<(unsigned)((R + kThreads / 32 - 1) / (kThreads / 32)), kThreads, 0, stream>>>(r, R);
+    route_permute_kernel<<<(unsigned)((R + kTileRows - 1) / kTileRows + r.E), kThreads, 0, stream>>>(r);
     return cudaGetLastError();
 }
 

@@ -70,12 +70,12 @@ def check_stagewise(d, E, k, F, dev, experts=None, weight_at_fc1=False, token_sa
                        ("perm", "perm", R), ("inv", "inv", R)]:
         assert np.array_equal(ws_np(ws, lay, name, np.int32, n), m[f]), name
 
-    # per-token quantization of X and the permute: exact bytes
+    # per-token quantization of X (block scales row-linear, the permute's input) and the
+    # permute (block scales swizzled, padded per expert): exact bytes
     xq_o = oracle.quantize(d["x"])
-    xq = DevQuant(ws[lay["xq_codes"]:lay["xq_codes"] + T * H // 2].view(T, H // 2),
-                  ws[lay["xq_sf"]:lay["xq_sf"] + oracle.sf_bytes(T, H // 16)],
-                  ws[lay["xq_scale"]:lay["xq_scale"] + 4 * T].view(torch.float32))
-    assert_quant_equal(xq, xq_o, T, H, what="xq")
+    assert np.array_equal(ws_np(ws, lay, "xq_codes", np.uint8, T * H // 2).reshape(T, H // 2), xq_o[0]), "xq codes"
+    assert np.array_equal(ws_np(ws, lay, "xq_sf", np.uint8, T * H // 16).reshape(T, H // 16), xq_o[1]), "xq sf"
+    assert np.array_equal(ws_np(ws, lay, "xq_scale", np.float32, T).view(np.uint32), xq_o[2].view(np.uint32))
     a1_o = oracle.permute(xq_o, m, k)
     prow = oracle.padded_rows(m)
     Rp = int(m["poff"][-1])
@@ -83,6 +83,11 @@ def check_stagewise(d, E, k, F, dev, experts=None, weight_at_fc1=False, token_sa
                   ws[lay["a1_sf"]:lay["a1_sf"] + Rp * H // 16],
                   ws[lay["a1_scale"]:lay["a1_scale"] + 4 * R].view(torch.float32))
     assert_quant_equal(a1, a1_o, R, H, row_map=prow, what="a1")
+    # the padding rows of each expert's last m-tile carry zero block scales
+    a1_all = oracle.sf_unswizzle(a1.sf.cpu().numpy(), Rp, H // 16)
+    pad = np.ones(Rp, bool)
+    pad[prow] = False
+    assert not a1_all[pad].any(), "a1 padding rows: nonzero block scales"
 
     off = m["off"]
     if experts is None:
