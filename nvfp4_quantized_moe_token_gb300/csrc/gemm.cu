@@ -36,7 +36,7 @@
 //                columns into registers, releases TMEM at once (arriving on
 //                the even CTA's barrier: the next tile's MMAs start), then
 //                scales and either converts to bf16 (mode 0) or computes
-//                SwiGLU -> bf16 D + row amax (mode 1).  Mode 0 outputs leave
+//                SwiGLU -> bf16 D + row amax (mode 1).  Outputs leave
 //                through a per-warp shared-memory box of 32 rows x 32 columns
 //                and a TMA tensor store; a warp whose 32 rows straddle the end
 //                of an expert group stores its valid rows directly.
@@ -70,27 +70,25 @@ constexpr int MAX_G = 256;
 constexpr uint32_t IDESC = idesc_nvfp4(2 * BM, BN);
 constexpr int STG_BYTES = 32 * 64;      // per-warp output staging box: 32 rows x 32 bf16
 
-// Pipeline shape per epilogue mode.  The plain (mode 0) epilogue writes a
-// full 128 x 256 bf16 tile per CTA per K loop of a few stages (FC2: K = 768),
-// so it takes 64-byte K-stages (8 in flight) and leaves room for the
-// TMA-store staging boxes.  The SwiGLU (mode 1) epilogue writes half as much
-// per much longer K loop (FC1: K = 2048): 128-byte K-stages (5 in flight,
-// more bytes per TMA request), direct stores.
+// Pipeline shape.  128-byte K-stages (4 MMAs per stage and per commit, so
+// the issuing thread's fixed cost per stage is spread over 512 tensor-pipe
+// cycles), 128B swizzle, 5 stages in flight, plus the epilogue's TMA-store
+// staging boxes (32 KB): together the 227 KB of shared memory.
 template <int MODE>
 struct Cfg {
-    static constexpr int BK = MODE == 0 ? 128 : 256;    // FP4 elements of K per stage
+    static constexpr int BK = 256;                      // FP4 elements of K per stage
     static constexpr int ROWB = BK / 2;                 // bytes per row per stage
-    static constexpr int STAGES = MODE == 0 ? 8 : 5;
+    static constexpr int STAGES = 5;
     static constexpr int A_BYTES = BM * ROWB;           // this CTA's 128 rows of A
     static constexpr int B_BYTES = 128 * ROWB;          // this CTA's half of the 256 weight rows
     static constexpr int ATOMS = BK / 64;               // scale atoms per 128 rows per stage
     static constexpr int SFA_BYTES = ATOMS * 512;
     static constexpr int SFB_BYTES = 2 * ATOMS * 512;   // weight scales of both halves
-    static constexpr int SWZ = MODE == 0 ? 4 : 2;       // descriptor swizzle code: 64B / 128B
+    static constexpr int SWZ = 2;                       // descriptor swizzle code: 128B
     static constexpr int SBO = 8 * ROWB;                // bytes between 8-row core-matrix groups
     static constexpr uint32_t SF_STAGE_COLS = 12 * ATOMS;  // SFA 4*ATOMS + SFB 8*ATOMS columns
-    static constexpr bool STAGED = MODE == 0;
-    static constexpr int NSTG = STAGED ? EPI_WARPS : 0;
+    static constexpr bool STAGED = true;
+    static constexpr int NSTG = EPI_WARPS;
     static_assert(SF_COL + STAGES * SF_STAGE_COLS <= TMEM_COLS, "scale columns exceed TMEM");
 };
 
@@ -114,6 +112,7 @@ struct __align__(1024) Smem {
     int gpoff[MAX_G + 1];
     int ppre[MAX_G + 1];           // units of m-tile pairs before each group
 };
+static_assert(sizeof(Smem<0>) + 1024 <= 232448 && sizeof(Smem<1>) + 1024 <= 232448, "shared memory per CTA");
 
 struct KParams {
     const uint8_t* a_sf;
@@ -322,6 +321,15 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
             // ------------------------------------------------------------ MMA issuer (even CTA)
+            // The issuing thread's instruction stream is kept short (it shares
+            // its scheduler with epilogue warps): descriptors of stage 0 are
+            // built once, a stage / K-step adds its byte offset >> 4 to the
+            // start-address field, and the K-steps are unrolled.  The wait on
+            // sf_full alone suffices: this CTA's scale writers arrive on it
+            // only after its own stage has landed, the peer's after the
+            // peer's stage has landed.
+            const uint64_t adesc0 = smem_desc(smem_u32(s.a[0]), 0, SBO, SWZ);
+            const uint64_t bdesc0 = smem_desc(smem_u32(s.b[0]), 0, SBO, SWZ);
             int stage = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
@@ -329,16 +337,17 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 if (!mbar_wait_bounded_cluster(smem_u32(&s.tmem_empty), acc_phase ^ 1, abort, p.err)) { ok = false; break; }
                 tc_fence_after();
                 for (int ks = 0; ks < k_stages; ++ks) {
-                    if (!mbar_wait_bounded(smem_u32(&s.full[stage]), phase, abort, p.err) ||
-                        !mbar_wait_bounded_cluster(smem_u32(&s.sf_full[stage]), phase, abort, p.err)) { ok = false; break; }
+                    if (!mbar_wait_bounded_cluster(smem_u32(&s.sf_full[stage]), phase, abort, p.err)) { ok = false; break; }
                     tc_fence_after();
-                    const int na = k_atoms - ks * ATOMS < ATOMS ? k_atoms - ks * ATOMS : ATOMS;
+                    const int na = k_atoms - ks * ATOMS;
                     const uint32_t sfc = tmem + SF_COL + stage * SF_STAGE_COLS;
-                    const uint32_t a0 = smem_u32(s.a[stage]), b0 = smem_u32(s.b[stage]);
-                    for (int kk = 0; kk < na; ++kk) {
-                        tc_mma2_nvfp4(tmem + ACC_COL, smem_desc(a0 + kk * 32, 0, SBO, SWZ),
-                                      smem_desc(b0 + kk * 32, 0, SBO, SWZ), IDESC,
-                                      sfc + kk * 4, sfc + 4 * ATOMS + kk * 8, (ks | kk) != 0);
+                    const uint64_t ad = adesc0 + (uint64_t)((stage * A_BYTES) >> 4);
+                    const uint64_t bd = bdesc0 + (uint64_t)((stage * B_BYTES) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < ATOMS; ++kk) {
+                        if (kk < na)
+                            tc_mma2_nvfp4(tmem + ACC_COL, ad + 2 * kk, bd + 2 * kk, IDESC, sfc + kk * 4,
+                                          sfc + 4 * ATOMS + kk * 8, (ks | kk) != 0);
                     }
                     tc_commit2_mc(smem_u32(&s.empty[stage]), 3);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
