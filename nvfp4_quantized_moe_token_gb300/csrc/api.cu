@@ -325,6 +325,7 @@ int moe_expert_forward(const void* x_bf16, int64_t T, int64_t H, const float* ro
     q2.goff = r.off;
     q2.gpoff = r.poff;
     q2.G = E;
+    q2.reverse = 1;  // FC1's last rows are still in L2; FC2 then starts on the rows written last
     q2.err = reinterpret_cast<uint32_t*>(at(L.err));
     if ((e = nvfp4::launch_quantize(q2, s)) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe requant: %s", cudaGetErrorString(e));
     if ((e = mark()) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe event: %s", cudaGetErrorString(e));

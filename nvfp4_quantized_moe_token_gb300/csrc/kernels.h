@@ -19,6 +19,7 @@ struct QuantLaunch {
     const int* goff;        // nullable: scale rows remapped by group padding
     const int* gpoff;
     int G;
+    int reverse;            // rows taken last to first
     void* ws;               // >= 4 bytes when per_tensor && !amax_in
     uint32_t* err;          // nullable device error word (pipeline wait time-outs)
 };

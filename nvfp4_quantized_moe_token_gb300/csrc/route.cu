@@ -179,9 +179,13 @@ constexpr int kTileRows = 128;
 __global__ void __launch_bounds__(kThreads) route_permute_kernel(RouteLaunch p) {
     __shared__ uint32_t ssf[kTileRows][33];  // [row][scale group], stride 33 words: no bank conflicts
     __shared__ int stok[kTileRows];
+    // tiles last to first: FC1 reads them first to last, and finds the ones
+    // written last still in L2
     const int E = p.E;
-    const int prow0 = blockIdx.x * kTileRows;
-    if (prow0 >= __ldg(p.poff + E)) return;
+    const int n_tiles = __ldg(p.poff + E) / kTileRows;
+    if ((int)blockIdx.x >= n_tiles) return;
+    const int tile = n_tiles - 1 - (int)blockIdx.x;
+    const int prow0 = tile * kTileRows;
     int lo = 0, hi = E;  // the expert whose padded rows hold prow0
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -217,7 +221,7 @@ __global__ void __launch_bounds__(kThreads) route_permute_kernel(RouteLaunch p) 
     // block scales, 32 groups of 4 (128 columns of scales) per pass
     const int64_t sp4 = p.H / 64;
     const int64_t sf_ld = p.H / 16;
-    uint8_t* tile_sf = p.a1_sf + (int64_t)blockIdx.x * sp4 * 512;
+    uint8_t* tile_sf = p.a1_sf + (int64_t)tile * sp4 * 512;
     for (int64_t q0 = 0; q0 < sp4; q0 += 32) {
         const int nq = sp4 - q0 < 32 ? (int)(sp4 - q0) : 32;
         for (int i = warp; i < kTileRows; i += W) {
