@@ -14,27 +14,30 @@ namespace {
 
 constexpr int kThreads = 256;
 
-__global__ void __launch_bounds__(kThreads) combine_kernel(CombineLaunch c) {
+// KMAX = the largest k the instance serves (registers for KMAX row loads):
+// 8 for the common top-8 routing (64 registers, 4 blocks per SM), else 16.
+template <int KMAX>
+__global__ void __launch_bounds__(kThreads, KMAX <= 8 ? 4 : 3) combine_kernel(CombineLaunch c) {
     const int64_t t = blockIdx.x;
     const __nv_bfloat16* y = reinterpret_cast<const __nv_bfloat16*>(c.y);
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(c.out) + t * c.H;
-    int row[16];
-    float w[16];
+    int row[KMAX];
+    float w[KMAX];
 #pragma unroll
-    for (int s = 0; s < 16; ++s) {
+    for (int s = 0; s < KMAX; ++s) {
         if (s < c.k) {
             row[s] = __ldg(c.inv + t * c.k + s);
             w[s] = c.w ? __ldg(c.w + t * c.k + s) : 1.0f;
         }
     }
     for (int64_t col = threadIdx.x * 8; col < c.H; col += kThreads * 8) {
-        uint4 v[16];
+        uint4 v[KMAX];
 #pragma unroll
-        for (int s = 0; s < 16; ++s)  // all k row loads in flight before any use
+        for (int s = 0; s < KMAX; ++s)  // all k row loads in flight before any use
             if (s < c.k) v[s] = __ldg(reinterpret_cast<const uint4*>(y + (int64_t)row[s] * c.H + col));
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
-        for (int s = 0; s < 16; ++s) {
+        for (int s = 0; s < KMAX; ++s) {
             if (s < c.k) {
                 const uint32_t wv[4] = {v[s].x, v[s].y, v[s].z, v[s].w};
 #pragma unroll
@@ -58,7 +61,8 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(CombineLaunch c) {
 
 cudaError_t launch_combine(const CombineLaunch& c, cudaStream_t stream) {
     if (c.T == 0) return cudaSuccess;
-    combine_kernel<<<(unsigned)c.T, kThreads, 0, stream>>>(c);
+    if (c.k <= 8) combine_kernel<8><<<(unsigned)c.T, kThreads, 0, stream>>>(c);
+    else combine_kernel<16><<<(unsigned)c.T, kThreads, 0, stream>>>(c);
     return cudaGetLastError();
 }
 

@@ -8,17 +8,19 @@
 // 128 experts ("miniTE Technical Report" 6.4 D15 profiles).
 //
 // Four kernels, all deterministic:
-//   1. route_topk: one warp per token -- z = logit + bias, k rounds of warp
-//      argmax (ties to the lower expert), softmax over the k selected z;
-//      per-chunk expert histogram in shared memory.
+//   1. route_topk: one warp per 4 tokens (their logits loaded together, their
+//      reductions interleaved) -- z = logit + bias, k rounds of warp argmax
+//      (ties to the lower expert), softmax over the k selected z; per-chunk
+//      expert histogram in shared memory.
 //   2. route_scan: one block per expert scans its chunk counts; the last
 //      block to finish turns the expert totals into offsets and padded
 //      offsets.
 //   3. route_scatter: one block per chunk of 32 tokens ranks each (token,
 //      slot) inside its expert by a shared-memory bitmap (stable: ascending
 //      token index) and writes perm / inv.
-//   4. route_permute: one warp per expert-ordered row copies the token's
-//      codes, scales and outer scale into the expert-ordered buffers.
+//   4. route_permute: one block per padded 128-row m-tile of an expert copies
+//      its rows' codes, block scales (staged in shared memory, written as
+//      whole swizzled atoms) and outer scales into the expert-ordered buffers.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -31,50 +33,70 @@ constexpr int kWarps = kThreads / 32;
 
 template <int EPL>  // experts per lane: E = 32 * EPL
 __global__ void __launch_bounds__(kThreads) route_topk_kernel(RouteLaunch p) {
+    constexpr int TPW = kRouteChunk / kWarps;  // tokens per warp, selected together
     __shared__ int scnt[32 * EPL];
     const int E = 32 * EPL;
     for (int e = threadIdx.x; e < E; e += kThreads) scnt[e] = 0;
     if (blockIdx.x == 0 && threadIdx.x == 0) *p.done = 0u;
     __syncthreads();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t t0 = (int64_t)blockIdx.x * kRouteChunk;
-    for (int i = warp; i < kRouteChunk; i += kWarps) {
-        const int64_t t = t0 + i;
-        if (t >= p.T) break;
-        float z[EPL];
+    const int64_t tw = (int64_t)blockIdx.x * kRouteChunk + warp * TPW;  // this warp's first token
+    // all logits of the warp's tokens in flight at once
+    float z[TPW][EPL];
+#pragma unroll
+    for (int u = 0; u < TPW; ++u) {
 #pragma unroll
         for (int j = 0; j < EPL; ++j) {
             const int e = lane + 32 * j;
             const float b = p.bias ? __ldg(p.bias + e) : 0.0f;
-            z[j] = __fadd_rn(__ldg(p.logits + t * E + e), b);
+            z[u][j] = tw + u < p.T ? __fadd_rn(__ldg(p.logits + (tw + u) * E + e), b) : 0.0f;
         }
-        uint32_t taken = 0;
-        float my_z = 0.0f;
-        int my_id = 0;
-        for (int s = 0; s < p.k; ++s) {
-            float bv = -INFINITY;
-            int bi = 0x7fffffff;
+    }
+    // k rounds of warp argmax (ties to the lower expert index), the TPW
+    // tokens' reductions interleaved so their shuffle latencies overlap
+    uint32_t taken[TPW];
+    float my_z[TPW];
+    int my_id[TPW];
+#pragma unroll
+    for (int u = 0; u < TPW; ++u) { taken[u] = 0u; my_z[u] = 0.0f; my_id[u] = 0; }
+    for (int s = 0; s < p.k; ++s) {
+        float bv[TPW];
+        int bi[TPW];
+#pragma unroll
+        for (int u = 0; u < TPW; ++u) {
+            bv[u] = -INFINITY;
+            bi[u] = 0x7fffffff;
 #pragma unroll
             for (int j = 0; j < EPL; ++j)
-                if (!((taken >> j) & 1u) && z[j] > bv) { bv = z[j]; bi = lane + 32 * j; }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-                if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-            }
-            if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-            if (lane == s) { my_z = bv; my_id = bi; }
+                if (!((taken[u] >> j) & 1u) && z[u][j] > bv[u]) { bv[u] = z[u][j]; bi[u] = lane + 32 * j; }
         }
-        // weights: softmax over the selected z, summed in slot order
-        const float zmax = __shfl_sync(0xffffffffu, my_z, 0);
-        const float ex = lane < p.k ? expf(__fsub_rn(my_z, zmax)) : 0.0f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+            for (int u = 0; u < TPW; ++u) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv[u], o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi[u], o);
+                if (ov > bv[u] || (ov == bv[u] && oi < bi[u])) { bv[u] = ov; bi[u] = oi; }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < TPW; ++u) {
+            if ((bi[u] & 31) == lane) taken[u] |= 1u << (bi[u] >> 5);
+            if (lane == s) { my_z[u] = bv[u]; my_id[u] = bi[u]; }
+        }
+    }
+    // weights: softmax over the selected z, summed in slot order
+#pragma unroll
+    for (int u = 0; u < TPW; ++u) {
+        const int64_t t = tw + u;
+        const float zmax = __shfl_sync(0xffffffffu, my_z[u], 0);
+        const float ex = lane < p.k ? expf(__fsub_rn(my_z[u], zmax)) : 0.0f;
         float sum = 0.0f;
         for (int s = 0; s < p.k; ++s) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, ex, s));
-        if (lane < p.k) {
-            p.ids[t * p.k + lane] = my_id;
+        if (t < p.T && lane < p.k) {
+            p.ids[t * p.k + lane] = my_id[u];
             p.w[t * p.k + lane] = __fdiv_rn(ex, sum);
-            atomicAdd(&scnt[my_id], 1);
+            atomicAdd(&scnt[my_id[u]], 1);
         }
     }
     __syncthreads();
