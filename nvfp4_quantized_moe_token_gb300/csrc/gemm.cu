@@ -72,13 +72,18 @@ constexpr int STG_BYTES = 32 * 64;      // per-warp output staging box: 32 rows 
 
 // Pipeline shape.  128-byte K-stages (4 MMAs per stage and per commit, so
 // the issuing thread's fixed cost per stage is spread over 512 tensor-pipe
-// cycles), 128B swizzle, 5 stages in flight, plus the epilogue's TMA-store
-// staging boxes (32 KB): together the 227 KB of shared memory.
+// cycles), 128B swizzle, plus the epilogue's TMA-store staging boxes.  The
+// SwiGLU epilogue (mode 1) stores one box per warp per tile of a long K
+// loop (FC1: 8 stages): 5 stages in flight, one box per warp.  The plain
+// epilogue (mode 0) stores two boxes per warp per tile of a short K loop
+// (FC2: 3 stages): 4 stages in flight and two boxes per warp, so a warp
+// fills its second box while the first is still being read by the TMA.
 template <int MODE>
 struct Cfg {
     static constexpr int BK = 256;                      // FP4 elements of K per stage
     static constexpr int ROWB = BK / 2;                 // bytes per row per stage
-    static constexpr int STAGES = 5;
+    static constexpr int STAGES = MODE == 0 ? 4 : 5;
+    static constexpr int NBUF = MODE == 0 ? 2 : 1;      // staging boxes per epilogue warp
     static constexpr int A_BYTES = BM * ROWB;           // this CTA's 128 rows of A
     static constexpr int B_BYTES = 128 * ROWB;          // this CTA's half of the 256 weight rows
     static constexpr int ATOMS = BK / 64;               // scale atoms per 128 rows per stage
@@ -88,7 +93,7 @@ struct Cfg {
     static constexpr int SBO = 8 * ROWB;                // bytes between 8-row core-matrix groups
     static constexpr uint32_t SF_STAGE_COLS = 12 * ATOMS;  // SFA 4*ATOMS + SFB 8*ATOMS columns
     static constexpr bool STAGED = true;
-    static constexpr int NSTG = EPI_WARPS;
+    static constexpr int NSTG = EPI_WARPS * NBUF;
     static_assert(SF_COL + STAGES * SF_STAGE_COLS <= TMEM_COLS, "scale columns exceed TMEM");
 };
 
@@ -175,13 +180,19 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 // One warp's 32 rows x 32 bf16 output columns (16 packed words per thread,
 // thread = row).  Whole warp inside the group: stage the box in shared memory
-// (64B-swizzled, as the tensor map expects) and issue one TMA tensor store;
-// otherwise each valid row is stored directly.
-template <bool STAGED>
-__device__ __forceinline__ void emit_box(const KParams& p, const CUtensorMap* tmO, uint32_t stg, const uint32_t* w,
-                                         bool full_warp, bool valid, int lane, int64_t row, int col, int row_base) {
+// (64B-swizzled, as the tensor map expects) in the next of the warp's NBUF
+// boxes and issue one TMA tensor store; otherwise each valid row is stored
+// directly.
+template <bool STAGED, int NBUF>
+__device__ __forceinline__ void emit_box(const KParams& p, const CUtensorMap* tmO, uint32_t stg_base, int& nbox,
+                                         const uint32_t* w, bool full_warp, bool valid, int lane, int64_t row,
+                                         int col, int row_base) {
     if (STAGED && full_warp) {
-        if (lane == 0) bulk_wait_read();  // the previous box of this warp has been read
+        const uint32_t stg = stg_base + (uint32_t)((nbox % NBUF) * STG_BYTES);
+        ++nbox;
+        if (lane == 0) {  // the store that last used this box has read it
+            if (NBUF == 2) bulk_wait_read_1(); else bulk_wait_read();
+        }
         __syncwarp();
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -203,11 +214,44 @@ __device__ __forceinline__ void emit_box(const KParams& p, const CUtensorMap* tm
     }
 }
 
-// silu(g) = g / (1 + exp(-g)) with the hardware exp2 and reciprocal
-// approximations (a few fp32 ulps, far inside the bf16 rounding that follows);
-// exp(-g) = inf for very negative g gives rcp = 0 and silu = -0, no NaN.
-__device__ __forceinline__ float silu(float g) {
-    return g * rcp_approx(1.0f + __expf(-g));
+// Pairs of fp32 values in one 64-bit register pair, for the packed
+// two-wide fp32 multiply and add (each lane rounded to nearest like the
+// scalar instruction), which halve the epilogue's multiply count.
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float f2_lo(uint64_t v) {
+    float a, b;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+    return a;
+}
+__device__ __forceinline__ float f2_hi(uint64_t v) {
+    float a, b;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+    return b;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(uint64_t v) { return pack_bf16(f2_lo(v), f2_hi(v)); }
+
+// silu(g) u for a pair: g / (1 + exp(-g)) with __expf and the hardware
+// reciprocal approximation (a few fp32 ulps, far inside the bf16 rounding
+// that follows); exp(-g) = inf for very negative g gives rcp = 0 and silu =
+// -0, no NaN.
+__device__ __forceinline__ uint64_t swiglu2(uint64_t g, uint64_t u) {
+    const uint64_t den = f2_add(f2(__expf(-f2_lo(g)), __expf(-f2_hi(g))), f2(1.0f, 1.0f));
+    const uint64_t sg = f2_mul(g, f2(rcp_approx(f2_lo(den)), rcp_approx(f2_hi(den))));
+    return f2_mul(sg, u);
 }
 
 template <int MODE>
@@ -405,6 +449,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         const uint32_t release = mapa_shared(smem_u32(&s.tmem_empty), 0);
         uint32_t acc_phase = 0;
         bool ok = true;
+        int nbox = 0;  // staged boxes this warp has stored
         for (int u = pair; u < total; u += n_pairs) {
             const Tile x = decode_unit(s, G, n_tiles, u, rank);
             const int rl = q * 32 + lane;
@@ -431,18 +476,19 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             acc_phase ^= 1;
             if (x.rows == 0) continue;  // the odd CTA of a group's last pair: nothing to store
             const float scale = __fmul_rn(sa, sbw);
+            const uint64_t scale2 = f2(scale, scale);
             // all 32 rows of this warp inside the tile's group: TMA store; else direct
             const bool full_warp = q * 32 + 32 <= x.rows;
-            const uint32_t stg = smem_u32(s.stg[C::NSTG > 0 ? warp - EPI_WARP0 : 0]);
+            const uint32_t stg = smem_u32(s.stg[(warp - EPI_WARP0) * C::NBUF]);
             if (MODE == 0) {
                 uint32_t w[32];  // convert all 64 values first: the fp32 registers die as they are packed
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
-                    w[j] = pack_bf16(__uint_as_float(v[2 * j]) * scale, __uint_as_float(v[2 * j + 1]) * scale);
+                    w[j] = pack_bf16x2(f2_mul(f2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), scale2));
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf)
-                    emit_box<C::STAGED>(p, &tmO, stg, w + hf * 16, full_warp, valid, lane, row,
-                                        x.nt * BN + cg * 64 + hf * 32, x.row0 + q * 32);
+                    emit_box<C::STAGED, C::NBUF>(p, &tmO, stg, nbox, w + hf * 16, full_warp, valid, lane, row,
+                                                 x.nt * BN + cg * 64 + hf * 32, x.row0 + q * 32);
             } else {
                 if (valid && p.c_debug) {
                     float* cgp = p.c_debug + row * p.N + x.nt * 128 + cg * 32;
@@ -459,21 +505,18 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 }
                 uint32_t w[16];
                 float m = 0.0f;
+                const uint64_t prob2 = f2(prob, prob);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    float d2[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const float g = __uint_as_float(v[2 * j + e]) * scale;
-                        const float u2 = __uint_as_float(v[32 + 2 * j + e]) * scale;
-                        float dv = silu(g) * u2;
-                        if (p.row_prob) dv *= prob;
-                        m = fmaxf(m, fabsf(dv));
-                        d2[e] = dv;
-                    }
-                    w[j] = pack_bf16(d2[0], d2[1]);
+                    const uint64_t g = f2_mul(f2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), scale2);
+                    const uint64_t u = f2_mul(f2(__uint_as_float(v[32 + 2 * j]), __uint_as_float(v[33 + 2 * j])), scale2);
+                    uint64_t dv = swiglu2(g, u);
+                    if (p.row_prob) dv = f2_mul(dv, prob2);
+                    m = fmaxf(m, fmaxf(fabsf(f2_lo(dv)), fabsf(f2_hi(dv))));
+                    w[j] = pack_bf16x2(dv);
                 }
-                emit_box<C::STAGED>(p, &tmO, stg, w, full_warp, valid, lane, row, x.nt * 128 + cg * 32, x.row0 + q * 32);
+                emit_box<C::STAGED, C::NBUF>(p, &tmO, stg, nbox, w, full_warp, valid, lane, row, x.nt * 128 + cg * 32,
+                                             x.row0 + q * 32);
                 // max |bf16(d)| = bf16(max |d|): rounding is monotone and odd
                 if (valid) {
                     const float mb = __bfloat162float(__float2bfloat16_rn(m));
