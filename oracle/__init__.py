@@ -53,6 +53,7 @@ def lib():
         L.orc_bf16_from_f64.argtypes = [ctypes.c_double]
         L.orc_bf16_from_f64_array.argtypes = [f64p, i64, u16p]
         L.orc_quantize.argtypes = [u16p, i64, i64, i64, i32, f32p, u8p, u8p, f32p]
+        L.orc_quantize_46.argtypes = [u16p, i64, i64, i64, i32, f32p, i32, u8p, u8p, f32p, u8p]
         L.orc_dequantize.argtypes = [u8p, u8p, f32p, i64, i64, i32, f64p]
         L.orc_sf_offset.restype = i64
         L.orc_sf_offset.argtypes = [i64, i64, i64]
@@ -135,6 +136,30 @@ def quantize(x_bf16, per_tensor=False, amax_in=None):
     lib().orc_quantize(_p(x, u16p), rows, cols, cols, int(per_tensor),
                        _p(am, f32p) if am is not None else None,
                        _p(codes, u8p), _p(sf, u8p), _p(scale, f32p))
+    return codes, sf, scale
+
+
+def quantize_46(x_bf16, err="mse", per_tensor=False, amax_in=None, with_choice=False):
+    """Four-over-six quantization (see orc_quantize_46): err 'mse' or 'mae'.
+
+    Returns (codes, sf_lin, scale) like quantize, plus the per-block choice
+    uint8 [rows, cols/16] (4 or 6) when with_choice."""
+    x = _c(x_bf16, np.uint16)
+    rows, cols = x.shape
+    assert cols % 16 == 0
+    kind = {"mse": 1, "mae": 2}[err]
+    codes = np.empty((rows, cols // 2), np.uint8)
+    sf = np.empty((rows, cols // 16), np.uint8)
+    scale = np.empty(1 if per_tensor else rows, np.float32)
+    choice = np.empty((rows, cols // 16), np.uint8)
+    am = None
+    if amax_in is not None:
+        am = _c(amax_in, np.float32).reshape(-1)
+    lib().orc_quantize_46(_p(x, u16p), rows, cols, cols, int(per_tensor),
+                          _p(am, f32p) if am is not None else None, kind,
+                          _p(codes, u8p), _p(sf, u8p), _p(scale, f32p), _p(choice, u8p))
+    if with_choice:
+        return codes, sf, scale, choice
     return codes, sf, scale
 
 

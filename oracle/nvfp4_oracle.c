@@ -237,6 +237,122 @@ void orc_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
     }
 }
 
+/* Four-over-six: per 16-block, the block max maps to 6 (the plain rule) or
+ * to 4, whichever encodes the block with the smaller error; 4 only when its
+ * error is strictly smaller.  [4bitter] "Four-Over-Six for RL Weights and
+ * Activations": a value near 5/6 of the range can be off by 1/6 of the range
+ * with max -> 6, by 1/8 with max -> 4; a candidate decodes as
+ * fp4_value * fp8_scale * amax / (E2M1_MAXVAL * E4M3_4OVER6_MAXVAL); the
+ * error of each candidate is summed per block (MSE or MAE) in fp32 against
+ * the target scaled down by the inverse of that factor, in FP32 accumulation.
+ *
+ * Readings (the pages name but do not print them):
+ *   E2M1_MAXVAL = 6, E4M3_4OVER6_MAXVAL = 256: the largest power of two whose
+ *     3/2 multiple (the block scale of a max -> 4 candidate) stays within
+ *     E4M3's 448.  So s_g = amax / 1536.
+ *   inv = 1536 / amax (fp32 division), target t_j = x_j * inv (fp32).
+ *   candidate c in {6, 4}: u = bmax / (c * s_g); s_b = E4M3(u); codes as in
+ *     orc_quantize with d = s_b * s_g; dq_j = e2m1(q_j) * s_b (exact);
+ *     diff_j = dq_j - t_j; err = sum over j = 0..15 in order of diff_j^2
+ *     (err_kind 1, MSE) or |diff_j| (err_kind 2, MAE), each step one fp32
+ *     operation (no fused multiply-add).
+ *   The row amax, zero rows and per-tensor mode as in orc_quantize.
+ * Outputs as orc_quantize, plus choice[rows x cols/16] = 4 or 6 (nullable). */
+static void encode_block(const uint16_t* xb, float s_g, float t, uint8_t* sb_out, uint8_t q[16]) {
+    float bmax = 0.0f, u, d, rcp = 0.0f;
+    int use_div;
+    uint8_t sb;
+    for (int j = 0; j < 16; ++j) {
+        float a = fabsf(bf16_to_f32(xb[j]));
+        if (a > bmax) bmax = a;
+    }
+    u = bmax / t;
+    sb = orc_e4m3_encode(u);
+    *sb_out = sb;
+    if (sb == 0) {
+        memset(q, 0, 16);
+        return;
+    }
+    d = (float)orc_e4m3_decode(sb) * s_g;
+    use_div = !(d >= FLT_MIN);
+    if (!use_div) rcp = 1.0f / d;
+    for (int j = 0; j < 16; ++j) {
+        float xv = bf16_to_f32(xb[j]);
+        q[j] = orc_e2m1_encode(use_div ? xv / d : xv * rcp);
+    }
+}
+
+static float block_error(const uint16_t* xb, uint8_t sb, const uint8_t q[16], float inv, int err_kind) {
+    float sbf = (float)orc_e4m3_decode(sb), err = 0.0f;
+    for (int j = 0; j < 16; ++j) {
+        float dq = (float)orc_e2m1_decode(q[j]) * sbf;
+        float tj = bf16_to_f32(xb[j]) * inv;
+        float diff = dq - tj;
+        err = err + (err_kind == 1 ? diff * diff : fabsf(diff));
+    }
+    return err;
+}
+
+void orc_quantize_46(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
+                     int per_tensor, const float* amax_in, int err_kind,
+                     uint8_t* codes, uint8_t* sf_lin, float* scale, uint8_t* choice) {
+    const int64_t nblk = cols / 16;
+    float tensor_amax = 0.0f;
+    if (per_tensor) {
+        if (amax_in) {
+            tensor_amax = amax_in[0];
+        } else {
+            for (int64_t r = 0; r < rows; ++r)
+                for (int64_t j = 0; j < cols; ++j) {
+                    float a = fabsf(bf16_to_f32(x[r * ld + j]));
+                    if (a > tensor_amax) tensor_amax = a;
+                }
+        }
+    }
+    for (int64_t r = 0; r < rows; ++r) {
+        const uint16_t* xr = x + r * ld;
+        uint8_t* cr = codes + r * (cols / 2);
+        uint8_t* sr = sf_lin + r * nblk;
+        float amax, s_g, inv;
+        if (per_tensor) {
+            amax = tensor_amax;
+        } else if (amax_in) {
+            amax = amax_in[r];
+        } else {
+            amax = 0.0f;
+            for (int64_t j = 0; j < cols; ++j) {
+                float a = fabsf(bf16_to_f32(xr[j]));
+                if (a > amax) amax = a;
+            }
+        }
+        s_g = amax / 1536.0f;
+        if (per_tensor) { if (r == 0) scale[0] = s_g; } else scale[r] = s_g;
+        if (s_g == 0.0f) {
+            memset(cr, 0, (size_t)(cols / 2));
+            memset(sr, 0, (size_t)nblk);
+            if (choice) memset(choice + r * nblk, 6, (size_t)nblk);
+            continue;
+        }
+        inv = 1536.0f / amax;
+        for (int64_t b = 0; b < nblk; ++b) {
+            const uint16_t* xb = xr + b * 16;
+            uint8_t sb6, sb4, q6[16], q4[16], *q;
+            float e6, e4;
+            int four;
+            encode_block(xb, s_g, 6.0f * s_g, &sb6, q6);
+            encode_block(xb, s_g, 4.0f * s_g, &sb4, q4);
+            e6 = block_error(xb, sb6, q6, inv, err_kind);
+            e4 = block_error(xb, sb4, q4, inv, err_kind);
+            four = e4 < e6;
+            q = four ? q4 : q6;
+            sr[b] = four ? sb4 : sb6;
+            if (choice) choice[r * nblk + b] = (uint8_t)(four ? 4 : 6);
+            for (int j = 0; j < 8; ++j)
+                cr[b * 8 + j] = (uint8_t)(q[2 * j] | (q[2 * j + 1] << 4));
+        }
+    }
+}
+
 /* Dequantize to fp64: out[r][j] = q * s_b * s_g (each product exact in fp64).
  * [miniTE] 2.2 decode rule. */
 void orc_dequantize(const uint8_t* codes, const uint8_t* sf_lin, const float* scale,
