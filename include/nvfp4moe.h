@@ -71,6 +71,12 @@ extern "C" {
 /* Scale modes of nvfp4_quantize_rows. */
 #define NVFP4_PER_ROW 0    /* one fp32 outer scale per row (per token) */
 #define NVFP4_PER_TENSOR 1 /* one fp32 outer scale for the whole matrix */
+/* Four-over-six block scaling, OR-ed into the scale mode (at most one of
+ * the two): per 16-block the max maps to 6 or to 4, whichever gives the
+ * smaller block error ("The 4-bitter Lesson", Four-Over-Six for RL Weights
+ * and Activations); see nvfp4_quantize_rows. */
+#define NVFP4_FOUR_OVER_SIX_MSE 2 /* error = sum of squared differences */
+#define NVFP4_FOUR_OVER_SIX_MAE 4 /* error = sum of absolute differences */
 
 /* Bits of the device error word. */
 #define NVFP4_DEVERR_TIMEOUT 1u   /* a pipeline wait (GEMM or quantizer) ran past its limit */
@@ -102,7 +108,7 @@ NVFP4_API size_t nvfp4_sf_bytes(int64_t rows, int64_t cols);
 
 /* Workspace bytes nvfp4_quantize_rows needs: 0 for NVFP4_PER_ROW, 256 for
  * NVFP4_PER_TENSOR (the tensor amax is reduced there when amax_in is not
- * given).  Pure host function. */
+ * given), with or without a four-over-six flag.  Pure host function. */
 NVFP4_API size_t nvfp4_quantize_workspace(int64_t rows, int64_t cols, int scale_mode);
 
 /*
@@ -120,6 +126,17 @@ NVFP4_API size_t nvfp4_quantize_workspace(int64_t rows, int64_t cols, int scale_
  *          an fp32 subnormal); code = E2M1_rne_saturating(v), sign kept.
  * Every step is an IEEE fp32 operation in that order, so the result is
  * bit-identical to any implementation of the same steps.
+ * With NVFP4_FOUR_OVER_SIX_MSE / _MAE ("The 4-bitter Lesson", Four-Over-Six
+ * for RL Weights and Activations; the pages name but do not print the E4M3
+ * ceiling, read here as 256):
+ *   s_g  = amax / 1536 (= 6 * 256, so a max -> 4 block scale, 3/2 of the
+ *          max -> 6 one, stays within E4M3's 448); inv = 1536 / amax.
+ *   per 16-block, for c = 6 and c = 4: s_b(c) = E4M3(bmax / (c s_g)) and
+ *          codes as above with d = s_b(c) s_g; err(c) = sum over j = 0..15
+ *          in order of (e2m1(q_j) s_b(c) - x_j inv)^2 (MSE) or |.| (MAE),
+ *          each step one fp32 operation; max -> 4 is kept only when
+ *          err(4) < err(6).
+ *   The decode rule is unchanged, so the GEMMs take such tensors as they are.
  * Shapes: rows >= 0, 0 < cols <= 32768, cols % 16 == 0, ld >= cols.
  * Alignment: x and ld*2 bytes 16-byte aligned; codes 16-byte aligned.
  * Scale-factor padding columns inside the last 4-column group are written 0;
@@ -152,6 +169,10 @@ typedef struct moe_options {
      * Technical Report" 5.3 weighted SwiGLU; the combine then sums the
      * expert outputs unweighted). */
     int weight_at_fc1;
+    /* 0, NVFP4_FOUR_OVER_SIX_MSE or NVFP4_FOUR_OVER_SIX_MAE: four-over-six
+     * block scaling of the activations (X and the FC2 input D).  Weights
+     * take it through their own nvfp4_quantize_rows call. */
+    int four_over_six;
 } moe_options;
 
 /* Optional debug outputs of moe_expert_forward (all nullable, device). */

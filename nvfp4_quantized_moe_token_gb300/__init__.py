@@ -25,7 +25,7 @@ class _Tensor(ctypes.Structure):
 
 
 class _Options(ctypes.Structure):
-    _fields_ = [("weight_at_fc1", ctypes.c_int)]
+    _fields_ = [("weight_at_fc1", ctypes.c_int), ("four_over_six", ctypes.c_int)]
 
 
 class _Debug(ctypes.Structure):
@@ -46,6 +46,7 @@ class _Layout(ctypes.Structure):
 
 PER_ROW = 0
 PER_TENSOR = 1
+FOUR_OVER_SIX = {None: 0, "mse": 2, "mae": 4}  # scale-mode flags of four-over-six block scaling
 SYMBOLS = ["nvfp4_sf_bytes", "nvfp4_quantize_workspace", "nvfp4_quantize_rows", "nvfp4_linear",
            "moe_expert_workspace_layout", "moe_expert_workspace", "moe_expert_forward",
            "moe_expert_forward_noalloc", "nvfp4_last_error"]
@@ -134,13 +135,14 @@ def sf_bytes(rows, cols):
     return int(lib().nvfp4_sf_bytes(rows, cols))
 
 
-def quantize_rows(x, per_tensor=False, amax_in=None, out=None, stream=None):
-    """bf16 [rows, cols] (CUDA) -> NVFP4Tensor (per-row or per-tensor outer scale)."""
+def quantize_rows(x, per_tensor=False, amax_in=None, out=None, four_over_six=None, stream=None):
+    """bf16 [rows, cols] (CUDA) -> NVFP4Tensor (per-row or per-tensor outer scale);
+    four_over_six None, 'mse' or 'mae' selects four-over-six block scaling."""
     assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
     rows, cols = x.shape
     if out is None:
         out = NVFP4Tensor.empty(rows, cols, 1 if per_tensor else rows, x.device)
-    mode = PER_TENSOR if per_tensor else PER_ROW
+    mode = (PER_TENSOR if per_tensor else PER_ROW) | FOUR_OVER_SIX[four_over_six]
     ws_bytes = int(lib().nvfp4_quantize_workspace(rows, cols, mode))
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=x.device) if ws_bytes else None
     t = out.c()
@@ -150,7 +152,7 @@ def quantize_rows(x, per_tensor=False, amax_in=None, out=None, stream=None):
     return out
 
 
-def quantize_grouped_weights(w, stream=None):
+def quantize_grouped_weights(w, four_over_six=None, stream=None):
     """Per-expert weights bf16 [G, N, K] -> one stacked NVFP4Tensor [G*N, K]
     with one per-tensor scale per expert (scale has G entries).  Requires
     N % 128 == 0 so each expert's swizzled scales are a contiguous slice."""
@@ -162,7 +164,8 @@ def quantize_grouped_weights(w, stream=None):
     for g in range(G):
         sub = _Tensor(out.codes.data_ptr() + g * N * (K // 2), out.sf.data_ptr() + g * per_sf,
                       out.scale.data_ptr() + 4 * g, N, K)
-        rc = lib().nvfp4_quantize_rows(_ptr(w[g]), N, K, K, PER_TENSOR, None, ctypes.byref(sub),
+        rc = lib().nvfp4_quantize_rows(_ptr(w[g]), N, K, K, PER_TENSOR | FOUR_OVER_SIX[four_over_six], None,
+                                       ctypes.byref(sub),
                                        _ptr(ws), 256, _stream(stream))
         _check(rc, "nvfp4_quantize_rows (weights)")
     return out
@@ -188,8 +191,9 @@ def moe_workspace_layout(T, H, F, E, topk):
 
 
 def moe_expert_forward(x, logits, bias, w1q, w2q, F, topk, weight_at_fc1=False, out=None,
-                       ws=None, fc1_debug=None, stage_events=None, stream=None):
+                       ws=None, fc1_debug=None, stage_events=None, four_over_six=None, stream=None):
     """One W4A4 MoE expert layer on the device.  Returns (out bf16 [T, H], ws).
+    four_over_six (None, 'mse', 'mae'): four-over-six scaling of the activations.
 
     stage_events (optional): len(STAGES) + 1 torch.cuda.Event objects recorded on
     the stream before the first stage and after each stage."""
@@ -201,7 +205,7 @@ def moe_expert_forward(x, logits, bias, w1q, w2q, F, topk, weight_at_fc1=False, 
     if out is None:
         out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
     a, b = w1q.c(), w2q.c()
-    opt = _Options(1 if weight_at_fc1 else 0)
+    opt = _Options(1 if weight_at_fc1 else 0, FOUR_OVER_SIX[four_over_six])
     evs = None
     if stage_events is not None:
         assert len(stage_events) == len(STAGES) + 1

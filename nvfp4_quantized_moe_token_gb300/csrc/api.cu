@@ -71,15 +71,28 @@ size_t nvfp4_sf_bytes(int64_t rows, int64_t cols) {
 size_t nvfp4_quantize_workspace(int64_t rows, int64_t cols, int scale_mode) {
     (void)rows;
     (void)cols;
-    return scale_mode == NVFP4_PER_TENSOR ? 256 : 0;
+    return (scale_mode & NVFP4_PER_TENSOR) ? 256 : 0;
 }
+
+namespace {
+// four-over-six selector of the quantizer (0 off, 1 MSE, 2 MAE) from the flags
+int fos_of(int flags) {
+    return (flags & NVFP4_FOUR_OVER_SIX_MSE) ? 1 : ((flags & NVFP4_FOUR_OVER_SIX_MAE) ? 2 : 0);
+}
+bool fos_flags_valid(int flags) {
+    return (flags & ~(NVFP4_FOUR_OVER_SIX_MSE | NVFP4_FOUR_OVER_SIX_MAE)) == 0 &&
+           (flags & (NVFP4_FOUR_OVER_SIX_MSE | NVFP4_FOUR_OVER_SIX_MAE)) !=
+               (NVFP4_FOUR_OVER_SIX_MSE | NVFP4_FOUR_OVER_SIX_MAE);
+}
+}  // namespace
 
 int nvfp4_quantize_rows(const void* x_bf16, int64_t rows, int64_t cols, int64_t ld, int scale_mode,
                         const float* amax_in, const nvfp4_tensor* out, void* ws, size_t ws_bytes,
                         void* stream) {
     if (x_bf16 == nullptr) return fail(NVFP4_EINVAL, "quantize: x is null");
-    if (scale_mode != NVFP4_PER_ROW && scale_mode != NVFP4_PER_TENSOR)
+    if (!fos_flags_valid(scale_mode & ~NVFP4_PER_TENSOR))
         return fail(NVFP4_EINVAL, "quantize: unknown scale_mode %d", scale_mode);
+    const bool per_tensor = (scale_mode & NVFP4_PER_TENSOR) != 0;
     int rc = check_tensor(out, "quantize out");
     if (rc) return rc;
     if (rows < 0 || cols <= 0 || ld < cols) return fail(NVFP4_EINVAL, "quantize: bad rows/cols/ld");
@@ -88,7 +101,7 @@ int nvfp4_quantize_rows(const void* x_bf16, int64_t rows, int64_t cols, int64_t 
     if (rows >= (1ll << 31) || cols > 32768) return fail(NVFP4_ESHAPE, "quantize: rows >= 2^31 or cols > 32768");
     if (!aligned(x_bf16, 16) || (ld % 8) != 0) return fail(NVFP4_EALIGN, "quantize: x and ld*2 must be 16-byte aligned");
     if (amax_in != nullptr && !aligned(amax_in, 4)) return fail(NVFP4_EALIGN, "quantize: amax_in misaligned");
-    if (scale_mode == NVFP4_PER_TENSOR && amax_in == nullptr && (ws == nullptr || ws_bytes < 256))
+    if (per_tensor && amax_in == nullptr && (ws == nullptr || ws_bytes < 256))
         return fail(NVFP4_EWORKSPACE, "quantize: per-tensor needs 256 bytes of ws");
     if (ws != nullptr && !aligned(ws, 16)) return fail(NVFP4_EALIGN, "quantize: ws must be 16-byte aligned");
     nvfp4::QuantLaunch q{};
@@ -97,7 +110,8 @@ int nvfp4_quantize_rows(const void* x_bf16, int64_t rows, int64_t cols, int64_t 
     q.rows = rows;
     q.cols = cols;
     q.amax_in = amax_in;
-    q.per_tensor = scale_mode == NVFP4_PER_TENSOR;
+    q.per_tensor = per_tensor;
+    q.fos = fos_of(scale_mode);
     q.codes = out->codes;
     q.sf = out->sf;
     q.scale = out->scale;
@@ -226,8 +240,13 @@ int moe_expert_forward(const void* x_bf16, int64_t T, int64_t H, const float* ro
         return fail(NVFP4_EWORKSPACE, "moe: workspace %zu < required %zu bytes", ws_bytes, L.total);
     if (dbg != nullptr && dbg->fc1_out != nullptr && !aligned(dbg->fc1_out, 16))
         return fail(NVFP4_EALIGN, "moe: dbg->fc1_out must be 16-byte aligned");
+    const int fos_flags = opt != nullptr ? opt->four_over_six : 0;
+    if (!fos_flags_valid(fos_flags) || (fos_flags != 0 && fos_flags != NVFP4_FOUR_OVER_SIX_MSE &&
+                                        fos_flags != NVFP4_FOUR_OVER_SIX_MAE))
+        return fail(NVFP4_EINVAL, "moe: four_over_six must be 0, NVFP4_FOUR_OVER_SIX_MSE or _MAE");
     if (sm_count() <= 0) return fail(NVFP4_ELAUNCH, "moe: no CUDA device");
     const bool at_fc1 = opt != nullptr && opt->weight_at_fc1 != 0;
+    const int fos = fos_of(fos_flags);
     uint8_t* base = reinterpret_cast<uint8_t*>(ws);
     auto at = [&](size_t off) { return base + off; };
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -251,6 +270,7 @@ int moe_expert_forward(const void* x_bf16, int64_t T, int64_t H, const float* ro
     qx.codes = at(L.xq_codes);
     qx.sf = at(L.xq_sf);
     qx.sf_ld = H / 16;  // row-linear: the permute gathers whole rows of scales
+    qx.fos = fos;
     qx.scale = reinterpret_cast<float*>(at(L.xq_scale));
     qx.err = reinterpret_cast<uint32_t*>(at(L.err));
     if ((e = nvfp4::launch_quantize(qx, s)) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe quantize: %s", cudaGetErrorString(e));
@@ -326,6 +346,7 @@ int moe_expert_forward(const void* x_bf16, int64_t T, int64_t H, const float* ro
     q2.gpoff = r.poff;
     q2.G = E;
     q2.reverse = 1;  // FC1's last rows are still in L2; FC2 then starts on the rows written last
+    q2.fos = fos;
     q2.err = reinterpret_cast<uint32_t*>(at(L.err));
     if ((e = nvfp4::launch_quantize(q2, s)) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe requant: %s", cudaGetErrorString(e));
     if ((e = mark()) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe event: %s", cudaGetErrorString(e));

@@ -20,6 +20,7 @@ struct QuantLaunch {
     const int* gpoff;
     int G;
     int reverse;            // rows taken last to first
+    int fos;                // four-over-six: 0 off, 1 by MSE, 2 by MAE
     void* ws;               // >= 4 bytes when per_tensor && !amax_in
     uint32_t* err;          // nullable device error word (pipeline wait time-outs)
 };

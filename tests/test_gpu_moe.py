@@ -25,11 +25,16 @@ class DevQuant:
         self.codes, self.sf, self.scale = codes, sf, scale
 
 
-def run_device(d, E, k, F, weight_at_fc1=False):
+def oq(x, fos, **kw):
+    """The oracle quantizer of a mode: plain, or four-over-six by 'mse' / 'mae'."""
+    return oracle.quantize(x, **kw) if fos is None else oracle.quantize_46(x, fos, **kw)
+
+
+def run_device(d, E, k, F, weight_at_fc1=False, fos=None, wfos=None):
     x = to_dev_bf16(d["x"])
     T, H = d["x"].shape
-    w1q = nv.quantize_grouped_weights(to_dev_bf16(d["w1"]))
-    w2q = nv.quantize_grouped_weights(to_dev_bf16(d["w2"]))
+    w1q = nv.quantize_grouped_weights(to_dev_bf16(d["w1"]), four_over_six=wfos)
+    w2q = nv.quantize_grouped_weights(to_dev_bf16(d["w2"]), four_over_six=wfos)
     logits = torch.from_numpy(d["logits"]).cuda()
     bias = torch.from_numpy(d["bias"]).cuda()
     R = T * k
@@ -37,10 +42,10 @@ def run_device(d, E, k, F, weight_at_fc1=False):
     need = nv.lib().moe_expert_workspace(T, H, F, E, k)
     ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
     out, ws = nv.moe_expert_forward(x, logits, bias, w1q, w2q, F, k, weight_at_fc1=weight_at_fc1,
-                                    ws=ws, fc1_debug=fc1)
+                                    ws=ws, fc1_debug=fc1, four_over_six=fos)
     torch.cuda.synchronize()
     return dict(out=bf16_bits(out), ws=ws, fc1=fc1, w1q=w1q, w2q=w2q,
-                lay=nv.moe_workspace_layout(T, H, F, E, k))
+                lay=nv.moe_workspace_layout(T, H, F, E, k), fos=fos, wfos=wfos)
 
 
 def ws_rows(ws, lay, field, dtype, R, C, rows):
@@ -72,7 +77,8 @@ def check_stagewise(d, E, k, F, dev, experts=None, weight_at_fc1=False, token_sa
 
     # per-token quantization of X (block scales row-linear, the permute's input) and the
     # permute (block scales swizzled, padded per expert): exact bytes
-    xq_o = oracle.quantize(d["x"])
+    fos, wfos = dev.get("fos"), dev.get("wfos")
+    xq_o = oq(d["x"], fos)
     assert np.array_equal(ws_np(ws, lay, "xq_codes", np.uint8, T * H // 2).reshape(T, H // 2), xq_o[0]), "xq codes"
     assert np.array_equal(ws_np(ws, lay, "xq_sf", np.uint8, T * H // 16).reshape(T, H // 16), xq_o[1]), "xq sf"
     assert np.array_equal(ws_np(ws, lay, "xq_scale", np.float32, T).view(np.uint32), xq_o[2].view(np.uint32))
@@ -112,8 +118,8 @@ def check_stagewise(d, E, k, F, dev, experts=None, weight_at_fc1=False, token_sa
             rng = np.random.default_rng(e)
             rows = np.unique(np.concatenate([rows[:64], rows[-64:], rng.choice(rows, 128, replace=False)]))
         # the expert's weights: device quantization bit-exact with the oracle's
-        w1e = oracle.quantize(d["w1"][e], per_tensor=True)
-        w2e = oracle.quantize(d["w2"][e], per_tensor=True)
+        w1e = oq(d["w1"][e], wfos, per_tensor=True)
+        w2e = oq(d["w2"][e], wfos, per_tensor=True)
         s1 = oracle.sf_bytes(2 * F, H // 16)
         s2 = oracle.sf_bytes(H, F // 16)
         assert np.array_equal(w1c[e * 2 * F:(e + 1) * 2 * F], w1e[0])
@@ -137,7 +143,7 @@ def check_stagewise(d, E, k, F, dev, experts=None, weight_at_fc1=False, token_sa
         assert np.all(np.abs(dg - do) <= oracle.bf16_ulp(np.maximum(np.abs(dg), np.abs(do)))), f"D expert {e}"
         assert np.array_equal(amax2[rows], np.abs(dg).max(axis=1).astype(np.float32)), f"amax2 expert {e}"
         # requant of the device's D with the reused amax: bit-exact
-        q2 = oracle.quantize(d_rows, amax_in=amax2[rows])
+        q2 = oq(d_rows, fos, amax_in=amax2[rows])
         assert np.array_equal(ws_rows(ws, lay, "a2_codes", np.uint8, R, F // 2, rows), q2[0]), f"q2 codes e{e}"
         assert np.array_equal(oracle.sf_unswizzle(a2sf, len(rows), F // 16, prow[rows]), q2[1]), f"q2 sf {e}"
         assert np.array_equal(a2s[rows].view(np.uint32), q2[2].view(np.uint32)), f"q2 scale {e}"
