@@ -14,12 +14,18 @@
 // receives its own 128 rows of the accumulator.  Per SM that halves the
 // weight bytes moved per tile (the single-CTA M=128 x N=256 form is limited
 // by the bytes it must stage, not by the tensor pipe), and one MMA issue
-// does the work of two.  Roles, 22 warps per CTA:
-//   warp 0       TMA producer (both CTAs): per K-stage its A tile (128 rows),
-//                its B half (128 rows) and the E4M3 scale atoms (plain bulk
-//                copies: the quantizer wrote them in the MMA's layout); the
-//                weight scales of both halves, since each SM's tensor core
-//                applies the scales of all 256 columns.
+// does the work of two.  Roles, 23 warps per CTA:
+//   warp 0       TMA producer of A (both CTAs): per K-stage its A tile (128
+//                rows, tensor copy) and the E4M3 scale atoms of those rows
+//                (a plain bulk copy: the quantizer wrote them in the MMA's
+//                layout).
+//   warp 22      TMA producer of B (both CTAs): per K-stage its half of the
+//                weight tile (128 rows) and the weight scales of both halves
+//                in one tensor copy (each SM's tensor core applies the scales
+//                of all 256 columns).  Every TMA instruction costs its
+//                issuing thread ~65-80 cycles, so the two operands are
+//                issued by two threads: one thread could not issue a K-stage's
+//                copies within the 512 cycles its MMAs take.
 //   warp 1       TMEM allocation (pair-collective, 512 columns) and, in the
 //                even CTA only, the MMA issuer: per stage tcgen05.mma
 //                .cta_group::2.kind::mxf4nvf4.block_scale (M=256, N=256,
@@ -33,8 +39,10 @@
 //                occupies the tensor pipe for ~55-80 cycles whatever its size;
 //                tcgen05.st runs on the warps.)
 //   warps 6-21   epilogue: each warp copies its 32 rows x 64 accumulator
-//                columns into registers, releases TMEM at once (arriving on
-//                the even CTA's barrier: the next tile's MMAs start), then
+//                columns into registers and arrives on a barrier of its CTA;
+//                warp 6 waits for all 16 and releases the CTA's half of TMEM
+//                with one arrival on the even CTA's barrier (the next tile's
+//                MMAs start), then each warp
 //                scales and either converts to bf16 (mode 0) or computes
 //                SwiGLU -> bf16 D + row amax (mode 1).  Outputs leave
 //                through a per-warp shared-memory box of 32 rows x 32 columns
@@ -62,7 +70,8 @@ constexpr int BM = 128;                 // rows per CTA (TMEM lanes); a pair cov
 constexpr int BN = 256;                 // accumulator columns per tile
 constexpr int EPI_WARP0 = 6;            // warps 2..5 write scales, 6..21 run the epilogue
 constexpr int EPI_WARPS = 16;
-constexpr int THREADS = (EPI_WARP0 + EPI_WARPS) * 32;
+constexpr int PRODB_WARP = EPI_WARP0 + EPI_WARPS;  // warp 22: producer of B
+constexpr int THREADS = (PRODB_WARP + 1) * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;
 constexpr uint32_t SF_COL = 256;
@@ -105,11 +114,13 @@ struct __align__(1024) Smem {
     uint8_t sfa[C::STAGES][C::SFA_BYTES];
     uint8_t sfb[C::STAGES][C::SFB_BYTES];
     uint8_t stg[C::NSTG > 0 ? C::NSTG : 1][C::NSTG > 0 ? STG_BYTES : 16];
-    uint64_t full[C::STAGES];      // this CTA's TMA bytes landed
+    uint64_t full_a[C::STAGES];    // this CTA's A tile and scales landed
+    uint64_t full_b[C::STAGES];    // this CTA's B half and the weight scales landed
     uint64_t sf_full[C::STAGES];   // (even CTA) scales of the stage in TMEM: 4 warps of each CTA
     uint64_t empty[C::STAGES];     // MMAs of the stage done (commit, multicast to the pair)
     uint64_t tmem_full;            // accumulator ready (commit, multicast to the pair)
-    uint64_t tmem_empty;           // (even CTA) accumulator drained: 16 warps of each CTA
+    uint64_t tmem_empty;           // (even CTA) accumulator drained: one arrival per CTA
+    uint64_t epi_done;             // this CTA's 16 epilogue warps copied the accumulator out
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -257,7 +268,8 @@ __device__ __forceinline__ uint64_t swiglu2(uint64_t g, uint64_t u) {
 template <int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                  const __grid_constant__ CUtensorMap tmO, const KParams p) {
+                  const __grid_constant__ CUtensorMap tmSFB, const __grid_constant__ CUtensorMap tmO,
+                  const KParams p) {
     using C = Cfg<MODE>;
     constexpr int STAGES = C::STAGES, A_BYTES = C::A_BYTES, B_BYTES = C::B_BYTES, ATOMS = C::ATOMS;
     constexpr int SFB_BYTES = C::SFB_BYTES, ROWB = C::ROWB, SWZ = C::SWZ, SBO = C::SBO;
@@ -280,17 +292,20 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     }
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
-            mbar_init(smem_u32(&s.full[i]), 1);
+            mbar_init(smem_u32(&s.full_a[i]), 1);
+            mbar_init(smem_u32(&s.full_b[i]), 1);
             mbar_init(smem_u32(&s.sf_full[i]), 8);
             mbar_init(smem_u32(&s.empty[i]), 1);
         }
         mbar_init(smem_u32(&s.tmem_full), 1);
-        mbar_init(smem_u32(&s.tmem_empty), 2 * EPI_WARPS);
+        mbar_init(smem_u32(&s.tmem_empty), 2);
+        mbar_init(smem_u32(&s.epi_done), EPI_WARPS);
         mbar_init(smem_u32(&s.drain), 1);
         s.abort = 0;
         fence_barrier_init();
     }
-    if (warp == 0 && lane == 0) { prefetch_tmap(&tmA); prefetch_tmap(&tmB); prefetch_tmap(&tmO); }
+    if (warp == 0 && lane == 0) { prefetch_tmap(&tmA); prefetch_tmap(&tmO); }
+    if (warp == PRODB_WARP && lane == 0) { prefetch_tmap(&tmB); prefetch_tmap(&tmSFB); }
     if (warp == 1) { tmem_alloc2(smem_u32(&s.tmem_base), TMEM_COLS); tmem_relinquish2(); }
     __syncthreads();
     if (warp == 0) {
@@ -327,39 +342,51 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const int k_atoms = p.K / 64;
     const int k_stages = (k_atoms + ATOMS - 1) / ATOMS;
 
-    if (warp == 0) {
+    if (warp == 0 || warp == PRODB_WARP) {
         if (lane == 0) {
-            // ------------------------------------------------------------ producer
-            int stage = 0;
+            // ------------------------------------------------------------ producers
+            // warp 0: A rows + their scales; warp 22: B half + weight scales
+            const bool is_a = warp == 0;
+            uint64_t* full = is_a ? s.full_a : s.full_b;
+            int stage = 0, issued = 0;
             uint32_t phase = 0;
-            int last_phase[STAGES];
-            for (int i = 0; i < STAGES; ++i) last_phase[i] = -1;
             bool ok = true;
             for (int u = pair; u < total && ok; u += n_pairs) {
                 const Tile x = decode_unit(s, G, n_tiles, u, rank);
+                // 128-row weight blocks of the pair's two halves: mode 1 takes
+                // 128 gate and 128 up rows of the expert, mode 0 two adjacent blocks
                 const int jb0 = MODE == 1 ? x.g * (p.N / 128) + x.nt : x.g * (p.N / 128) + 2 * x.nt;
                 const int jb1 = MODE == 1 ? x.g * (p.N / 128) + p.N / 256 + x.nt : jb0 + 1;
                 const int jb = rank == 0 ? jb0 : jb1;
                 for (int ks = 0; ks < k_stages; ++ks) {
                     if (!mbar_wait_bounded(smem_u32(&s.empty[stage]), phase ^ 1, abort, p.err)) { ok = false; break; }
-                    const int na = k_atoms - ks * ATOMS < ATOMS ? k_atoms - ks * ATOMS : ATOMS;
-                    const uint32_t fb = smem_u32(&s.full[stage]);
-                    mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES + 3 * na * 512);
-                    tma_load_2d(smem_u32(s.a[stage]), &tmA, fb, ks * ROWB, x.row0);
-                    tma_load_2d(smem_u32(s.b[stage]), &tmB, fb, ks * ROWB, jb * 128);
-                    bulk_load(smem_u32(s.sfa[stage]), p.a_sf + ((int64_t)x.mt * k_atoms + ks * ATOMS) * 512, na * 512, fb);
-                    bulk_load(smem_u32(s.sfb[stage]), p.b_sf + ((int64_t)jb0 * k_atoms + ks * ATOMS) * 512, na * 512, fb);
-                    bulk_load(smem_u32(s.sfb[stage]) + SFB_BYTES / 2,
-                              p.b_sf + ((int64_t)jb1 * k_atoms + ks * ATOMS) * 512, na * 512, fb);
-                    last_phase[stage] = (int)phase;
+                    const uint32_t fb = smem_u32(&full[stage]);
+                    if (is_a) {
+                        const int na = k_atoms - ks * ATOMS < ATOMS ? k_atoms - ks * ATOMS : ATOMS;
+                        mbar_arrive_expect_tx(fb, A_BYTES + na * 512);
+                        tma_load_2d(smem_u32(s.a[stage]), &tmA, fb, ks * ROWB, x.row0);
+                        bulk_load(smem_u32(s.sfa[stage]), p.a_sf + ((int64_t)x.mt * k_atoms + ks * ATOMS) * 512,
+                                  na * 512, fb);
+                    } else {
+                        // the scale box is always whole: atoms past K are zero-filled
+                        mbar_arrive_expect_tx(fb, B_BYTES + SFB_BYTES);
+                        tma_load_2d(smem_u32(s.b[stage]), &tmB, fb, ks * ROWB, jb * 128);
+                        if (MODE == 1)
+                            tma_load_4d(smem_u32(s.sfb[stage]), &tmSFB, fb, 0, ks * ATOMS, x.nt, 2 * x.g);
+                        else
+                            tma_load_3d(smem_u32(s.sfb[stage]), &tmSFB, fb, 0, ks * ATOMS, jb0);
+                    }
+                    ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
             }
             if (!ok) {
                 raise_abort(&s.abort, rank);
                 // drain: the last load issued into each stage has landed (bounded wait)
-                for (int st = 0; st < STAGES; ++st)
-                    if (last_phase[st] >= 0) mbar_wait_drain(smem_u32(&s.full[st]), (uint32_t)last_phase[st]);
+                for (int st = 0; st < STAGES && st < issued; ++st) {
+                    const int idx = st + (issued - 1 - st) / STAGES * STAGES;  // last stage issued into slot st
+                    mbar_wait_drain(smem_u32(&full[st]), (uint32_t)(idx / STAGES) & 1u);
+                }
             }
         }
     } else if (warp == 1) {
@@ -370,18 +397,18 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             // built once, a stage / K-step adds its byte offset >> 4 to the
             // start-address field, and the K-steps are unrolled.  The wait on
             // sf_full alone suffices: this CTA's scale writers arrive on it
-            // only after its own stage has landed, the peer's after the
-            // peer's stage has landed.
+            // only after both of its stage's copies have landed, the peer's
+            // after the peer's have.
             const uint64_t adesc0 = smem_desc(smem_u32(s.a[0]), 0, SBO, SWZ);
             const uint64_t bdesc0 = smem_desc(smem_u32(s.b[0]), 0, SBO, SWZ);
             int stage = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
             for (int u = pair; u < total && ok; u += n_pairs) {
-                if (!mbar_wait_bounded_cluster(smem_u32(&s.tmem_empty), acc_phase ^ 1, abort, p.err)) { ok = false; break; }
+                if (!mbar_wait_bounded_relaxed(smem_u32(&s.tmem_empty), acc_phase ^ 1, abort, p.err)) { ok = false; break; }
                 tc_fence_after();
                 for (int ks = 0; ks < k_stages; ++ks) {
-                    if (!mbar_wait_bounded_cluster(smem_u32(&s.sf_full[stage]), phase, abort, p.err)) { ok = false; break; }
+                    if (!mbar_wait_bounded_relaxed(smem_u32(&s.sf_full[stage]), phase, abort, p.err)) { ok = false; break; }
                     tc_fence_after();
                     const int na = k_atoms - ks * ATOMS;
                     const uint32_t sfc = tmem + SF_COL + stage * SF_STAGE_COLS;
@@ -419,7 +446,8 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         bool ok = true;
         for (int u = pair; u < total && ok; u += n_pairs) {
             for (int ks = 0; ks < k_stages; ++ks) {
-                if (!mbar_wait_bounded(smem_u32(&s.full[stage]), phase, abort, p.err)) { ok = false; break; }
+                if (!mbar_wait_bounded(smem_u32(&s.full_a[stage]), phase, abort, p.err) ||
+                    !mbar_wait_bounded(smem_u32(&s.full_b[stage]), phase, abort, p.err)) { ok = false; break; }
                 const uint32_t sfc = lane_addr + SF_COL + stage * SF_STAGE_COLS;
 #pragma unroll
                 for (int kk = 0; kk < ATOMS; ++kk) {
@@ -438,11 +466,11 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             }
         }
         if (!ok && lane == 0) raise_abort(&s.abort, rank);
-    } else {
+    } else if (warp < PRODB_WARP) {
         // ---------------------------------------------------------------- epilogue
-        // Each warp copies its 32 rows x 64 accumulator columns into registers
-        // and releases TMEM at once, so the next tile's MMAs run while this
-        // warp scales, activates and stores.
+        // Each warp copies its 32 rows x 64 accumulator columns into registers;
+        // once all 16 have, warp 6 releases the CTA's TMEM with one arrival, so
+        // the next tile's MMAs run while the warps scale, activate and store.
         const int q = warp & 3;                    // TMEM lane quarter this warp may access
         const int cg = (warp - EPI_WARP0) >> 2;    // column group 0..3
         const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
@@ -459,7 +487,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             const float sa = valid ? __ldg(p.a_scale + row) : 0.0f;
             const float sbw = __ldg(p.b_scale + x.g);
             const float prob = (valid && p.row_prob) ? __ldg(p.row_prob + row) : 1.0f;
-            if (!mbar_wait_bounded_cluster(smem_u32(&s.tmem_full), acc_phase, abort, p.err)) { ok = false; break; }
+            if (!mbar_wait_bounded_relaxed(smem_u32(&s.tmem_full), acc_phase, abort, p.err)) { ok = false; break; }
             tc_fence_after();
             uint32_t v[64];
             if (MODE == 0) {
@@ -472,7 +500,19 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(release);
+            if (lane == 0) mbar_arrive(smem_u32(&s.epi_done));
+            if (warp == EPI_WARP0) {
+                if (lane == 0) {
+                    if (mbar_wait_bounded(smem_u32(&s.epi_done), acc_phase, abort, p.err)) {
+                        tc_fence_after();
+                        mbar_arrive_cluster(release);
+                    } else {
+                        ok = false;
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                if (!ok) break;
+            }
             acc_phase ^= 1;
             if (x.rows == 0) continue;  // the odd CTA of a group's last pair: nothing to store
             const float scale = __fmul_rn(sa, sbw);
@@ -573,6 +613,34 @@ bool make_codes_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Weight scales, stored as 128-row blocks of k_atoms 512-byte atoms, viewed
+// as 32-bit words so one tensor copy brings a stage's atoms of the pair's two
+// 128-row blocks: mode 0 (adjacent blocks jb, jb + 1) as 3D {128, k_atoms,
+// G*N/128} with box {128, ATOMS, 2}; mode 1 (gate block nt and up block
+// N/256 + nt of expert g) as 4D {128, k_atoms, N/256, 2G} with box {128,
+// ATOMS, 1, 2}, the up block being one step of the last dimension away.
+bool make_sfb_map(CUtensorMap* m, const void* base, int G, int N, int K, int mode) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t k_atoms = (cuuint64_t)(K / 64);
+    const cuuint32_t atoms = (cuuint32_t)(mode == 0 ? Cfg<0>::ATOMS : Cfg<1>::ATOMS);
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    if (mode == 0) {
+        cuuint64_t dims[3] = {128, k_atoms, (cuuint64_t)G * (N / 128)};
+        cuuint64_t strides[2] = {512, k_atoms * 512};
+        cuuint32_t box[3] = {128, atoms, 2};
+        return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
+    cuuint64_t dims[4] = {128, k_atoms, (cuuint64_t)(N / 256), 2 * (cuuint64_t)G};
+    cuuint64_t strides[3] = {512, k_atoms * 512, k_atoms * 512 * (cuuint64_t)(N / 256)};
+    cuuint32_t box[4] = {128, atoms, 1, 2};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2D bf16 view [rows x cols] (row stride ld elements) of an output, 32 x 32 boxes, 64B swizzle.
 bool make_out_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld) {
     EncodeTiledFn fn = encode_fn();
@@ -610,7 +678,8 @@ int resident_pairs(size_t smem, int num_sms) {
 }
 
 template <int MODE>
-cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const KParams& p,
+cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsfb, const CUtensorMap& to,
+                        const KParams& p,
                         int num_sms, int64_t dense_units, cudaStream_t stream) {
     const size_t smem = sizeof(Smem<MODE>) + 1024;
     static std::mutex mu;
@@ -632,7 +701,7 @@ cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
     }
     if (dense_units > 0 && dense_units < pairs) pairs = (int)dense_units;
     if (pairs < 1) pairs = 1;
-    gemm_nvfp4_kernel<MODE><<<2 * pairs, THREADS, smem, stream>>>(ta, tb, to, p);
+    gemm_nvfp4_kernel<MODE><<<2 * pairs, THREADS, smem, stream>>>(ta, tb, tsfb, to, p);
     return cudaGetLastError();
 }
 
@@ -650,9 +719,10 @@ int device_sm_count() {
 
 cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
     if (g.M <= 0) return cudaSuccess;
-    CUtensorMap ta, tb, to;
+    CUtensorMap ta, tb, tsfb, to;
     if (!make_codes_map(&ta, g.a_codes, g.M, g.K / 2, g.mode)) return cudaErrorInvalidValue;
     if (!make_codes_map(&tb, g.b_codes, (int64_t)g.G * g.N, g.K / 2, g.mode)) return cudaErrorInvalidValue;
+    if (!make_sfb_map(&tsfb, g.b_sf, g.goff ? g.G : 1, g.N, g.K, g.mode)) return cudaErrorInvalidValue;
     const int64_t out_cols = g.mode == 1 ? g.N / 2 : g.N;
     if (!make_out_map(&to, g.out, g.M, out_cols, g.ldo)) return cudaErrorInvalidValue;
     KParams p;
@@ -676,8 +746,8 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
     const int num_sms = g.num_sms > 0 ? g.num_sms : 148;
     // dense calls: no more pairs than units of work (m-tile pairs x n-tiles)
     const int64_t dense_units = g.goff == nullptr ? ((g.M + BM - 1) / BM + 1) / 2 * (g.N / BN) : 0;
-    if (g.mode == 0) return launch_mode<0>(ta, tb, to, p, num_sms, dense_units, stream);
-    return launch_mode<1>(ta, tb, to, p, num_sms, dense_units, stream);
+    if (g.mode == 0) return launch_mode<0>(ta, tb, tsfb, to, p, num_sms, dense_units, stream);
+    return launch_mode<1>(ta, tb, tsfb, to, p, num_sms, dense_units, stream);
 }
 
 }  // namespace nvfp4
