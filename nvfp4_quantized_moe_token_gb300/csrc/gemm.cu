@@ -255,14 +255,40 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
 }
 __device__ __forceinline__ uint32_t pack_bf16x2(uint64_t v) { return pack_bf16(f2_lo(v), f2_hi(v)); }
 
-// silu(g) u for a pair: g / (1 + exp(-g)) with __expf and the hardware
-// reciprocal approximation (a few fp32 ulps, far inside the bf16 rounding
-// that follows); exp(-g) = inf for very negative g gives rcp = 0 and silu =
-// -0, no NaN.
-__device__ __forceinline__ uint64_t swiglu2(uint64_t g, uint64_t u) {
-    const uint64_t den = f2_add(f2(__expf(-f2_lo(g)), __expf(-f2_hi(g))), f2(1.0f, 1.0f));
-    const uint64_t sg = f2_mul(g, f2(rcp_approx(f2_lo(den)), rcp_approx(f2_hi(den))));
-    return f2_mul(sg, u);
+__device__ __forceinline__ float ex2_approx(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// silu(g) u for a pair from the accumulators a_g, a_u and the row's scale:
+// g = a_g s, u = a_u s, exp(-g) = 2^(a_g e) with e = -s log2(e) (the
+// hardware exp2 and reciprocal approximations: a few fp32 ulps, far inside
+// the bf16 rounding that follows); exp(-g) = inf for very negative g gives
+// rcp = 0 and silu = -0, no NaN.
+__device__ __forceinline__ uint64_t swiglu2(uint64_t ag, uint64_t au, uint64_t scale2, uint64_t escale2) {
+    const uint64_t ea = f2_mul(ag, escale2);
+    const uint64_t den = f2_add(f2(ex2_approx(f2_lo(ea)), ex2_approx(f2_hi(ea))), f2(1.0f, 1.0f));
+    const uint64_t sg = f2_mul(f2_mul(ag, scale2), f2(rcp_approx(f2_lo(den)), rcp_approx(f2_hi(den))));
+    return f2_mul(sg, f2_mul(au, scale2));
+}
+
+// One 16-pair SwiGLU pass of an epilogue warp: bf16 D words and the running
+// max of their magnitudes (bf16 magnitude bits order like unsigned integers,
+// so a packed 16-bit max of the stored values gives max |bf16(d)| exactly).
+template <bool PROB>
+__device__ __forceinline__ uint32_t swiglu_words(const uint32_t* v, uint64_t scale2, uint64_t escale2, uint64_t prob2,
+                                                 uint32_t* w) {
+    uint32_t mw = 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        uint64_t dv = swiglu2(f2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])),
+                              f2(__uint_as_float(v[32 + 2 * j]), __uint_as_float(v[33 + 2 * j])), scale2, escale2);
+        if (PROB) dv = f2_mul(dv, prob2);
+        w[j] = pack_bf16x2(dv);
+        mw = __vmaxu2(mw, w[j] & 0x7FFF7FFFu);
+    }
+    return mw;
 }
 
 template <int MODE>
@@ -544,22 +570,16 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     }
                 }
                 uint32_t w[16];
-                float m = 0.0f;
-                const uint64_t prob2 = f2(prob, prob);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const uint64_t g = f2_mul(f2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), scale2);
-                    const uint64_t u = f2_mul(f2(__uint_as_float(v[32 + 2 * j]), __uint_as_float(v[33 + 2 * j])), scale2);
-                    uint64_t dv = swiglu2(g, u);
-                    if (p.row_prob) dv = f2_mul(dv, prob2);
-                    m = fmaxf(m, fmaxf(fabsf(f2_lo(dv)), fabsf(f2_hi(dv))));
-                    w[j] = pack_bf16x2(dv);
-                }
+                const float es = __fmul_rn(scale, -1.44269504088896341f);
+                const uint64_t escale2 = f2(es, es);
+                uint32_t mw = p.row_prob ? swiglu_words<true>(v, scale2, escale2, f2(prob, prob), w)
+                                         : swiglu_words<false>(v, scale2, escale2, 0, w);
                 emit_box<C::STAGED, C::NBUF>(p, &tmO, stg, nbox, w, full_warp, valid, lane, row, x.nt * 128 + cg * 32,
                                              x.row0 + q * 32);
-                // max |bf16(d)| = bf16(max |d|): rounding is monotone and odd
+                // the row's max |bf16(d)| over this warp's 32 columns
                 if (valid) {
-                    const float mb = __bfloat162float(__float2bfloat16_rn(m));
+                    mw = __vmaxu2(mw, mw >> 16);
+                    const float mb = __uint_as_float((mw & 0xFFFFu) << 16);
                     atomicMax(reinterpret_cast<unsigned int*>(p.amax_out + row), __float_as_uint(mb));
                 }
             }
