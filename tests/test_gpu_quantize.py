@@ -110,3 +110,26 @@ def test_quant_row_scale_sweep():
     x = workloads.to_bf16_bits(base * np.exp2(k).astype(np.float32)[:, None])
     got, ref = run_both(x)
     assert_quant_equal(got, ref, rows, cols, what="scale sweep")
+
+
+def test_quant_strided_and_offset_rows():
+    """Rows read through a row stride of cols + 8 and from a base 16 bytes
+    past a 32-byte boundary: the quantizer's 16-byte load path (one 32-byte
+    load per block is taken only for 32-byte aligned rows)."""
+    rng = np.random.default_rng(29)
+    rows, cols = 300, 2048
+    x = workloads.gaussian_bf16(rng, (rows, cols), outlier_frac=0.01, zero_row_frac=0.05)
+    wide = np.zeros((rows, cols + 8), np.uint16)
+    wide[:, :cols] = x
+    dev = to_dev_bf16(wide)[:, :cols]
+    assert dev.stride(0) == cols + 8
+    got = nv.quantize_rows(dev)
+    torch.cuda.synchronize()
+    assert_quant_equal(got, oracle.quantize(x), rows, cols, what="row stride cols + 8")
+    flat = np.zeros(rows * cols + 8, np.uint16)
+    flat[8:] = x.reshape(-1)
+    dev = to_dev_bf16(flat)[8:].view(rows, cols)
+    assert dev.data_ptr() % 32 == 16
+    got = nv.quantize_rows(dev)
+    torch.cuda.synchronize()
+    assert_quant_equal(got, oracle.quantize(x), rows, cols, what="base 16 bytes off a 32-byte boundary")
