@@ -192,8 +192,9 @@ def algorithmic(R):
     b16, f32 = 2, 4
     q_row = H // 2 + H // 16 + f32
     return {
-        "quantize": ("hbm", T * H * b16 + T * q_row),
-        "route": ("hbm", T * E * f32 + E * f32 + T * K_TOP * 8 + T * q_row + R * q_row + R * 8),
+        # the router top-k runs in the quantize launch (independent work, one launch)
+        "quantize": ("hbm", T * H * b16 + T * q_row + T * E * f32 + E * f32 + T * K_TOP * 8),
+        "route": ("hbm", T * q_row + R * q_row + R * 8),
         "fc1": ("tensor", 2.0 * R * (2 * F) * H),
         "requant": ("hbm", R * F * b16 + R * f32 + R * (F // 2 + F // 16 + f32)),
         "fc2": ("tensor", 2.0 * R * H * F),

@@ -181,8 +181,9 @@ typedef struct moe_debug {
      * the alpha scaling, before SwiGLU (gate columns then up columns). */
     float* fc1_out;
     /* MOE_STAGE_EVENTS cudaEvent_t handles (created by the caller) recorded
-     * on `stream` before the first stage and after each stage: quantize X,
-     * route + permute, FC1, requant, FC2, combine. */
+     * on `stream` before the first stage and after each stage: quantize X
+     * (with the router top-k, launched together), routing metadata +
+     * permute, FC1, requant, FC2, combine. */
     void** stage_events;
 } moe_debug;
 

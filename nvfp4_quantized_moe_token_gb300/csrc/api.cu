@@ -261,7 +261,8 @@ int moe_expert_forward(const void* x_bf16, int64_t T, int64_t H, const float* ro
     if ((e = mark()) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe event: %s", cudaGetErrorString(e));
 
     // 1. per-token quantization of X (once per token; the permute moves the
-    //    result, scales row-linear here and swizzled in the permuted copy)
+    //    result, scales row-linear here and swizzled in the permuted copy),
+    //    in the same launch as the router top-k: the two are independent
     nvfp4::QuantLaunch qx{};
     qx.x = x_bf16;
     qx.ld = H;
@@ -273,8 +274,6 @@ int moe_expert_forward(const void* x_bf16, int64_t T, int64_t H, const float* ro
     qx.fos = fos;
     qx.scale = reinterpret_cast<float*>(at(L.xq_scale));
     qx.err = reinterpret_cast<uint32_t*>(at(L.err));
-    if ((e = nvfp4::launch_quantize(qx, s)) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe quantize: %s", cudaGetErrorString(e));
-    if ((e = mark()) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe event: %s", cudaGetErrorString(e));
 
     // 2. routing, metadata and permute
     nvfp4::RouteLaunch r{};
@@ -304,7 +303,11 @@ int moe_expert_forward(const void* x_bf16, int64_t T, int64_t H, const float* ro
     r.a1_scale = reinterpret_cast<float*>(at(L.a1_scale));
     r.amax2 = reinterpret_cast<float*>(at(L.amax2));
     r.row_w = at_fc1 ? reinterpret_cast<float*>(at(L.row_weights)) : nullptr;
-    if ((e = nvfp4::launch_route(r, s)) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe route: %s", cudaGetErrorString(e));
+
+    if ((e = nvfp4::launch_quantize_topk(qx, r, s)) != cudaSuccess)
+        return fail(NVFP4_ELAUNCH, "moe quantize + top-k: %s", cudaGetErrorString(e));
+    if ((e = mark()) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe event: %s", cudaGetErrorString(e));
+    if ((e = nvfp4::launch_route_rest(r, s)) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe route: %s", cudaGetErrorString(e));
     if ((e = mark()) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe event: %s", cudaGetErrorString(e));
 
     // 3. FC1 grouped GEMM, SwiGLU + row-amax epilogue

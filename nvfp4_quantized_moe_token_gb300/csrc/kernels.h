@@ -82,7 +82,13 @@ struct RouteLaunch {
     float* row_w;          // nullable: [T*k] router weight of each expert-ordered row
 };
 constexpr int kRouteChunk = 32;  // tokens per chunk of the stable scatter (one bitmap word)
-cudaError_t launch_route(const RouteLaunch& r, cudaStream_t stream);
+cudaError_t launch_route(const RouteLaunch& r, cudaStream_t stream);       // top-k, then the rest
+cudaError_t launch_route_topk(const RouteLaunch& r, cudaStream_t stream);  // top-k + chunk histograms
+cudaError_t launch_route_rest(const RouteLaunch& r, cudaStream_t stream);  // scan, scatter, permute
+// Per-token quantization of X and the router top-k in one launch (their
+// blocks interleaved: independent work, both latency-bound); separate
+// launches where the shapes fall outside the fused instances.
+cudaError_t launch_quantize_topk(const QuantLaunch& q, const RouteLaunch& r, cudaStream_t stream);
 
 struct CombineLaunch {
     const void* y;         // bf16 [R x H]

@@ -8,10 +8,10 @@
 // 128 experts ("miniTE Technical Report" 6.4 D15 profiles).
 //
 // Four kernels, all deterministic:
-//   1. route_topk: one warp per 4 tokens (their logits loaded together, their
-//      reductions interleaved) -- z = logit + bias, k rounds of warp argmax
-//      (ties to the lower expert), softmax over the k selected z; per-chunk
-//      expert histogram in shared memory.
+//   1. route_topk (route_topk.cuh; in the expert layer it shares one launch
+//      with the quantization of X): one warp per 4 tokens -- z = logit +
+//      bias, k rounds of warp argmax (ties to the lower expert), softmax over
+//      the k selected z; per-chunk expert histogram in shared memory.
 //   2. route_scan: one block per expert scans its chunk counts; the last
 //      block to finish turns the expert totals into offsets and padded
 //      offsets.
@@ -23,6 +23,7 @@
 //      whole swizzled atoms) and outer scales into the expert-ordered buffers.
 #include "common.cuh"
 #include "kernels.h"
+#include "route_topk.cuh"
 
 namespace nvfp4 {
 
@@ -31,76 +32,9 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
-template <int EPL>  // experts per lane: E = 32 * EPL
-__global__ void __launch_bounds__(kThreads) route_topk_kernel(RouteLaunch p) {
-    constexpr int TPW = kRouteChunk / kWarps;  // tokens per warp, selected together
-    __shared__ int scnt[32 * EPL];
-    const int E = 32 * EPL;
-    for (int e = threadIdx.x; e < E; e += kThreads) scnt[e] = 0;
-    if (blockIdx.x == 0 && threadIdx.x == 0) *p.done = 0u;
-    __syncthreads();
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t tw = (int64_t)blockIdx.x * kRouteChunk + warp * TPW;  // this warp's first token
-    // all logits of the warp's tokens in flight at once
-    float z[TPW][EPL];
-#pragma unroll
-    for (int u = 0; u < TPW; ++u) {
-#pragma unroll
-        for (int j = 0; j < EPL; ++j) {
-            const int e = lane + 32 * j;
-            const float b = p.bias ? __ldg(p.bias + e) : 0.0f;
-            z[u][j] = tw + u < p.T ? __fadd_rn(__ldg(p.logits + (tw + u) * E + e), b) : 0.0f;
-        }
-    }
-    // k rounds of warp argmax (ties to the lower expert index), the TPW
-    // tokens' reductions interleaved so their shuffle latencies overlap
-    uint32_t taken[TPW];
-    float my_z[TPW];
-    int my_id[TPW];
-#pragma unroll
-    for (int u = 0; u < TPW; ++u) { taken[u] = 0u; my_z[u] = 0.0f; my_id[u] = 0; }
-    for (int s = 0; s < p.k; ++s) {
-        float bv[TPW];
-        int bi[TPW];
-#pragma unroll
-        for (int u = 0; u < TPW; ++u) {
-            bv[u] = -INFINITY;
-            bi[u] = 0x7fffffff;
-#pragma unroll
-            for (int j = 0; j < EPL; ++j)
-                if (!((taken[u] >> j) & 1u) && z[u][j] > bv[u]) { bv[u] = z[u][j]; bi[u] = lane + 32 * j; }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-#pragma unroll
-            for (int u = 0; u < TPW; ++u) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv[u], o);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi[u], o);
-                if (ov > bv[u] || (ov == bv[u] && oi < bi[u])) { bv[u] = ov; bi[u] = oi; }
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < TPW; ++u) {
-            if ((bi[u] & 31) == lane) taken[u] |= 1u << (bi[u] >> 5);
-            if (lane == s) { my_z[u] = bv[u]; my_id[u] = bi[u]; }
-        }
-    }
-    // weights: softmax over the selected z, summed in slot order
-#pragma unroll
-    for (int u = 0; u < TPW; ++u) {
-        const int64_t t = tw + u;
-        const float zmax = __shfl_sync(0xffffffffu, my_z[u], 0);
-        const float ex = lane < p.k ? expf(__fsub_rn(my_z[u], zmax)) : 0.0f;
-        float sum = 0.0f;
-        for (int s = 0; s < p.k; ++s) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, ex, s));
-        if (t < p.T && lane < p.k) {
-            p.ids[t * p.k + lane] = my_id[u];
-            p.w[t * p.k + lane] = __fdiv_rn(ex, sum);
-            atomicAdd(&scnt[my_id[u]], 1);
-        }
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += kThreads) p.chunk_cnt[(int64_t)blockIdx.x * E + e] = scnt[e];
+template <int EPL>
+__global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(RouteLaunch p) {
+    route_topk_block<EPL>(p, blockIdx.x);
 }
 
 // Block-wide exclusive scan of one int per thread (kThreads threads).
@@ -264,23 +198,26 @@ __global__ void __launch_bounds__(kThreads) route_permute_kernel(RouteLaunch p) 
 
 }  // namespace
 
-cudaError_t launch_route(const RouteLaunch& r, cudaStream_t stream) {
+cudaError_t launch_route_topk(const RouteLaunch& r, cudaStream_t stream) {
     const int nchunks = (int)((r.T + kRouteChunk - 1) / kRouteChunk);
     switch (r.E / 32) {
-        case 1: route_topk_kernel<1><<<nchunks, kThreads, 0, stream>>>(r); break;
-        case 2: route_topk_kernel<2><<<nchunks, kThreads, 0, stream>>>(r); break;
-        case 3: route_topk_kernel<3><<<nchunks, kThreads, 0, stream>>>(r); break;
-        case 4: route_topk_kernel<4><<<nchunks, kThreads, 0, stream>>>(r); break;
-        case 5: route_topk_kernel<5><<<nchunks, kThreads, 0, stream>>>(r); break;
-        case 6: route_topk_kernel<6><<<nchunks, kThreads, 0, stream>>>(r); break;
-        case 7: route_topk_kernel<7><<<nchunks, kThreads, 0, stream>>>(r); break;
-        case 8: route_topk_kernel<8><<<nchunks, kThreads, 0, stream>>>(r); break;
+        case 1: route_topk_kernel<1><<<nchunks, kTopkThreads, 0, stream>>>(r); break;
+        case 2: route_topk_kernel<2><<<nchunks, kTopkThreads, 0, stream>>>(r); break;
+        case 3: route_topk_kernel<3><<<nchunks, kTopkThreads, 0, stream>>>(r); break;
+        case 4: route_topk_kernel<4><<<nchunks, kTopkThreads, 0, stream>>>(r); break;
+        case 5: route_topk_kernel<5><<<nchunks, kTopkThreads, 0, stream>>>(r); break;
+        case 6: route_topk_kernel<6><<<nchunks, kTopkThreads, 0, stream>>>(r); break;
+        case 7: route_topk_kernel<7><<<nchunks, kTopkThreads, 0, stream>>>(r); break;
+        case 8: route_topk_kernel<8><<<nchunks, kTopkThreads, 0, stream>>>(r); break;
         default: return cudaErrorInvalidValue;  // E is validated by the caller
     }
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_route_rest(const RouteLaunch& r, cudaStream_t stream) {
+    const int nchunks = (int)((r.T + kRouteChunk - 1) / kRouteChunk);
     route_scan_kernel<<<r.E, kThreads, 0, stream>>>(r, nchunks);
-    e = cudaGetLastError();
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     route_scatter_kernel<<<nchunks, kThreads, sizeof(uint32_t) * r.E, stream>>>(r);
     e = cudaGetLastError();
@@ -289,6 +226,12 @@ cudaError_t launch_route(const RouteLaunch& r, cudaStream_t stream) {
     const int64_t R = r.T * r.k;
     route_permute_kernel<<<(unsigned)((R + kTileRows - 1) / kTileRows + r.E), kThreads, 0, stream>>>(r);
     return cudaGetLastError();
+}
+
+cudaError_t launch_route(const RouteLaunch& r, cudaStream_t stream) {
+    cudaError_t e = launch_route_topk(r, stream);
+    if (e != cudaSuccess) return e;
+    return launch_route_rest(r, stream);
 }
 
 }  // namespace nvfp4
