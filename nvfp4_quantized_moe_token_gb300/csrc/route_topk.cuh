@@ -4,10 +4,11 @@
 // independent of it.
 //
 // "miniTE Technical Report" 6.4 (D15 profiles): top-8 of 128 experts.  One
-// warp per 4 tokens (their logits loaded together, their reductions
-// interleaved): z = logit + bias, k rounds of warp argmax (ties to the lower
-// expert), softmax over the k selected z; per-chunk expert histogram in
-// shared memory.  Blocks of kTopkThreads threads.
+// warp per 4 tokens (their logits loaded together, their rounds
+// interleaved): z = logit + bias, k rounds of warp argmax on order-preserving
+// integer keys (ties to the lower expert), softmax over the k selected z;
+// per-chunk expert histogram in shared memory.  Blocks of kTopkThreads
+// threads.
 #pragma once
 
 #include "common.cuh"
@@ -40,38 +41,58 @@ __device__ __forceinline__ void route_topk_block(const RouteLaunch& p, int chunk
         }
     }
     // k rounds of warp argmax (ties to the lower expert index), the TPW
-    // tokens' reductions interleaved so their shuffle latencies overlap
-    uint32_t taken[TPW];
-    float my_z[TPW];
-    int my_id[TPW];
+    // tokens' rounds interleaved.  Each z becomes a 32-bit key that orders
+    // like the float (sign bit flipped for z >= 0, all bits for z < 0; -0 is
+    // first made +0 so that equal values share one key), so a round is one
+    // warp max of keys and one warp min of the indices holding it
+    // (redux.sync), not a five-level shuffle reduction.  Taken entries count
+    // as key 0, below every value.
+    uint32_t key[TPW][EPL];
 #pragma unroll
-    for (int u = 0; u < TPW; ++u) { taken[u] = 0u; my_z[u] = 0.0f; my_id[u] = 0; }
-    for (int s = 0; s < p.k; ++s) {
-        float bv[TPW];
-        int bi[TPW];
+    for (int u = 0; u < TPW; ++u) {
 #pragma unroll
-        for (int u = 0; u < TPW; ++u) {
-            bv[u] = -INFINITY;
-            bi[u] = 0x7fffffff;
-#pragma unroll
-            for (int j = 0; j < EPL; ++j)
-                if (!((taken[u] >> j) & 1u) && z[u][j] > bv[u]) { bv[u] = z[u][j]; bi[u] = lane + 32 * j; }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-#pragma unroll
-            for (int u = 0; u < TPW; ++u) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv[u], o);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi[u], o);
-                if (ov > bv[u] || (ov == bv[u] && oi < bi[u])) { bv[u] = ov; bi[u] = oi; }
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < TPW; ++u) {
-            if ((bi[u] & 31) == lane) taken[u] |= 1u << (bi[u] >> 5);
-            if (lane == s) { my_z[u] = bv[u]; my_id[u] = bi[u]; }
+        for (int j = 0; j < EPL; ++j) {
+            const uint32_t b = __float_as_uint(__fadd_rn(z[u][j], 0.0f));
+            key[u][j] = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
         }
     }
+    uint32_t taken[TPW], my_key[TPW];
+    int my_id[TPW];
+#pragma unroll
+    for (int u = 0; u < TPW; ++u) { taken[u] = 0u; my_key[u] = 0u; my_id[u] = 0; }
+    for (int s = 0; s < p.k; ++s) {
+        uint32_t m[TPW];
+#pragma unroll
+        for (int u = 0; u < TPW; ++u) {
+            uint32_t lm = 0u;
+#pragma unroll
+            for (int j = 0; j < EPL; ++j)
+                if (!((taken[u] >> j) & 1u)) lm = max(lm, key[u][j]);
+            m[u] = lm;
+        }
+#pragma unroll
+        for (int u = 0; u < TPW; ++u) m[u] = __reduce_max_sync(0xffffffffu, m[u]);
+        uint32_t bi[TPW];
+#pragma unroll
+        for (int u = 0; u < TPW; ++u) {
+            uint32_t c = 0xffffffffu;  // this lane's lowest expert index holding the max
+#pragma unroll
+            for (int j = EPL - 1; j >= 0; --j)
+                if (!((taken[u] >> j) & 1u) && key[u][j] == m[u]) c = (uint32_t)(lane + 32 * j);
+            bi[u] = c;
+        }
+#pragma unroll
+        for (int u = 0; u < TPW; ++u) bi[u] = __reduce_min_sync(0xffffffffu, bi[u]);
+#pragma unroll
+        for (int u = 0; u < TPW; ++u) {
+            if ((int)(bi[u] & 31u) == lane) taken[u] |= 1u << (bi[u] >> 5);
+            if (lane == s) { my_key[u] = m[u]; my_id[u] = (int)bi[u]; }
+        }
+    }
+    float my_z[TPW];
+#pragma unroll
+    for (int u = 0; u < TPW; ++u)
+        my_z[u] = __uint_as_float((my_key[u] & 0x80000000u) ? (my_key[u] & 0x7fffffffu) : ~my_key[u]);
     // weights: softmax over the selected z, summed in slot order
 #pragma unroll
     for (int u = 0; u < TPW; ++u) {

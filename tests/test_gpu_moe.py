@@ -178,7 +178,8 @@ def small_layer(T, E, k, H, F, seed, bias_std=1.0):
                 w2=workloads.gaussian_bf16(rng, (E, H, F), std=0.02))
 
 
-@pytest.mark.parametrize("T,E,k,H,F", [(1000, 32, 4, 512, 256), (1, 32, 2, 256, 128), (129, 64, 8, 256, 384)])
+@pytest.mark.parametrize("T,E,k,H,F", [(1000, 32, 4, 512, 256), (1, 32, 2, 256, 128), (129, 64, 8, 256, 384),
+                                         (129, 128, 8, 1024, 128), (33, 128, 8, 2048, 256)])
 def test_moe_small_full_and_end_to_end(T, E, k, H, F):
     d = small_layer(T, E, k, H, F, seed=T + E)
     dev = run_device(d, E, k, F)
@@ -241,3 +242,21 @@ def test_moe_qwen3_shapes_stagewise(name):
     experts = _pick_experts(m, 4, 0)
     toks = np.random.default_rng(1).choice(d["x"].shape[0], 2048, replace=False)
     check_stagewise(d, E, k, F, dev, experts=experts, token_sample=toks)
+
+
+def test_moe_router_ties_and_signed_zeros():
+    """Logits from a handful of values (exact ties everywhere, +0 and -0
+    among them) through the 128-expert layer whose top-k shares a launch with
+    the quantization of X: ids must match the oracle's lower-index tie rule
+    exactly (-0 and +0 are one value), and the rest of the layer with it."""
+    T, E, k, H, F = 512, 128, 8, 1024, 128
+    rng = np.random.default_rng(17)
+    d = small_layer(T, E, k, H, F, seed=17)
+    vals = np.array([-1.0, -0.0, 0.0, 0.5, 1.0, 2.0], np.float32)
+    d["logits"] = vals[rng.integers(0, len(vals), (T, E))]
+    d["bias"] = np.zeros(E, np.float32)
+    d["bias"][::7] = np.float32(-0.0)
+    dev = run_device(d, E, k, F)
+    ids_o, _ = oracle.route(d["logits"], d["bias"], k)
+    m = oracle.route_metadata(ids_o, E)
+    check_stagewise(d, E, k, F, dev, experts=_pick_experts(m, 3, 2))
