@@ -57,6 +57,7 @@
 // flight and lets both CTAs exit normally (TMEM freed).
 #include <cuda.h>
 
+#include <cstddef>
 #include <mutex>
 
 #include "common.cuh"
@@ -67,7 +68,6 @@ namespace nvfp4 {
 namespace {
 
 constexpr int BM = 128;                 // rows per CTA (TMEM lanes); a pair covers 2 * BM
-constexpr int BN = 256;                 // accumulator columns per tile
 constexpr int EPI_WARP0 = 6;            // warps 2..5 write scales, 6..21 run the epilogue
 constexpr int EPI_WARPS = 16;
 constexpr int PRODB_WARP = EPI_WARP0 + EPI_WARPS;  // warp 22: producer of B
@@ -76,33 +76,47 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;
 constexpr uint32_t SF_COL = 256;
 constexpr int MAX_G = 256;
-constexpr uint32_t IDESC = idesc_nvfp4(2 * BM, BN);
-constexpr int STG_BYTES = 32 * 64;      // per-warp output staging box: 32 rows x 32 bf16
 
 // Pipeline shape.  128-byte K-stages (4 MMAs per stage and per commit, so
-// the issuing thread's fixed cost per stage is spread over 512 tensor-pipe
-// cycles), 128B swizzle, plus the epilogue's TMA-store staging boxes.  The
-// SwiGLU epilogue (mode 1) stores one box per warp per tile of a long K
-// loop (FC1: 8 stages): 5 stages in flight, one box per warp.  The plain
-// epilogue (mode 0) stores two boxes per warp per tile of a short K loop
-// (FC2: 3 stages): 4 stages in flight and two boxes per warp, so a warp
-// fills its second box while the first is still being read by the TMA.
+// the issuing thread's fixed cost per stage is spread over the stage's
+// tensor-pipe cycles), 128B swizzle, plus the epilogue's TMA-store staging
+// boxes.
+// Mode 1 (SwiGLU, FC1: a long K loop of 8 stages): 256-column tiles (128
+// gate + 128 up), one accumulator, 5 stages in flight, one box per warp.
+// Mode 0 (plain, FC2: a short K loop of 3 stages): 256-column tiles, one
+// accumulator, 4 stages, and each epilogue warp's 32 x 64 output block
+// leaves as one TMA store of 128-byte rows (128B swizzle) from one staging
+// box.  Measured on FC2 and dropped: 128-column tiles with two accumulators
+// (the next tile's MMAs running while the epilogue drains; 0.37 ms against
+// 0.31: twice the A tile loads and epilogue passes), 32 x 32 boxes of 64-byte
+// rows (0.31 ms), stores from the warps instead of the TMA (coalesced full
+// lines read back from the staging box: 0.38 ms).  The tile shape is a
+// parameter (TN, ACC_BUFS): both forms pass the parity tests.
 template <int MODE>
 struct Cfg {
     static constexpr int BK = 256;                      // FP4 elements of K per stage
     static constexpr int ROWB = BK / 2;                 // bytes per row per stage
+    static constexpr int TN = 256;                      // accumulator columns per tile
+    static constexpr int ACC_BUFS = 1;                  // accumulators in TMEM (2 fit at TN = 128)
+    static constexpr int B_ROWS = TN / 2;               // weight rows staged per CTA (half the tile)
+    static constexpr int SFB_BLOCKS = TN / 128;         // 128-row weight-scale blocks per tile
     static constexpr int STAGES = MODE == 0 ? 4 : 5;
-    static constexpr int NBUF = MODE == 0 ? 2 : 1;      // staging boxes per epilogue warp
+    static constexpr int NBUF = 1;                      // staging boxes per epilogue warp
     static constexpr int A_BYTES = BM * ROWB;           // this CTA's 128 rows of A
-    static constexpr int B_BYTES = 128 * ROWB;          // this CTA's half of the 256 weight rows
+    static constexpr int B_BYTES = B_ROWS * ROWB;       // this CTA's half of the weight rows
     static constexpr int ATOMS = BK / 64;               // scale atoms per 128 rows per stage
     static constexpr int SFA_BYTES = ATOMS * 512;
-    static constexpr int SFB_BYTES = 2 * ATOMS * 512;   // weight scales of both halves
+    static constexpr int SFB_BYTES = SFB_BLOCKS * ATOMS * 512;  // weight scales of the whole tile
     static constexpr int SWZ = 2;                       // descriptor swizzle code: 128B
     static constexpr int SBO = 8 * ROWB;                // bytes between 8-row core-matrix groups
-    static constexpr uint32_t SF_STAGE_COLS = 12 * ATOMS;  // SFA 4*ATOMS + SFB 8*ATOMS columns
+    static constexpr uint32_t SF_STAGE_COLS = 4 * ATOMS * (1 + SFB_BLOCKS);  // SFA 4 + SFB 4 per block, per atom
+    static constexpr uint32_t IDESC = idesc_nvfp4(2 * BM, TN);
+    static constexpr int BOXW = MODE == 0 ? TN / 4 : 32;  // output columns per epilogue warp = store box width
+    static constexpr int STG_BYTES = 32 * BOXW * 2;       // one staging box: 32 rows x BOXW bf16
     static constexpr bool STAGED = true;
+    static constexpr bool TMA_STORE = true;               // false: coalesced warp stores from the staging box
     static constexpr int NSTG = EPI_WARPS * NBUF;
+    static_assert(ACC_BUFS * TN <= (int)SF_COL, "accumulators overlap the scale columns");
     static_assert(SF_COL + STAGES * SF_STAGE_COLS <= TMEM_COLS, "scale columns exceed TMEM");
 };
 
@@ -113,14 +127,14 @@ struct __align__(1024) Smem {
     uint8_t b[C::STAGES][C::B_BYTES];
     uint8_t sfa[C::STAGES][C::SFA_BYTES];
     uint8_t sfb[C::STAGES][C::SFB_BYTES];
-    uint8_t stg[C::NSTG > 0 ? C::NSTG : 1][C::NSTG > 0 ? STG_BYTES : 16];
+    uint8_t stg[C::NSTG > 0 ? C::NSTG : 1][C::NSTG > 0 ? C::STG_BYTES : 16];
     uint64_t full_a[C::STAGES];    // this CTA's A tile and scales landed
     uint64_t full_b[C::STAGES];    // this CTA's B half and the weight scales landed
     uint64_t sf_full[C::STAGES];   // (even CTA) scales of the stage in TMEM: 4 warps of each CTA
     uint64_t empty[C::STAGES];     // MMAs of the stage done (commit, multicast to the pair)
-    uint64_t tmem_full;            // accumulator ready (commit, multicast to the pair)
-    uint64_t tmem_empty;           // (even CTA) accumulator drained: one arrival per CTA
-    uint64_t epi_done;             // this CTA's 16 epilogue warps copied the accumulator out
+    uint64_t tmem_full[C::ACC_BUFS];   // accumulator ready (commit, multicast to the pair)
+    uint64_t tmem_empty[C::ACC_BUFS];  // (even CTA) accumulator drained: one arrival per CTA
+    uint64_t epi_done[C::ACC_BUFS];    // this CTA's 16 epilogue warps copied that accumulator out
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -129,6 +143,8 @@ struct __align__(1024) Smem {
     int ppre[MAX_G + 1];           // units of m-tile pairs before each group
 };
 static_assert(sizeof(Smem<0>) + 1024 <= 232448 && sizeof(Smem<1>) + 1024 <= 232448, "shared memory per CTA");
+// the staging boxes start on 1024-byte boundaries (the TMA swizzle patterns repeat per 1024 bytes)
+static_assert(offsetof(Smem<0>, stg) % 1024 == 0 && offsetof(Smem<1>, stg) % 1024 == 0, "staging alignment");
 
 struct KParams {
     const uint8_t* a_sf;
@@ -189,39 +205,61 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// One warp's 32 rows x 32 bf16 output columns (16 packed words per thread,
-// thread = row).  Whole warp inside the group: stage the box in shared memory
-// (64B-swizzled, as the tensor map expects) in the next of the warp's NBUF
-// boxes and issue one TMA tensor store; otherwise each valid row is stored
-// directly.
-template <bool STAGED, int NBUF>
+// One warp's 32 rows x BOXW bf16 output columns (BOXW / 2 packed words per
+// thread, thread = row).  Whole warp inside the group: stage the box in
+// shared memory (swizzled as the tensor map expects: 64B for 64-byte rows,
+// 128B for 128-byte rows) in the next of the warp's NBUF boxes and issue one
+// TMA tensor store; otherwise each valid row is stored directly.
+template <bool STAGED, int NBUF, int BOXW, bool TMA_STORE>
 __device__ __forceinline__ void emit_box(const KParams& p, const CUtensorMap* tmO, uint32_t stg_base, int& nbox,
                                          const uint32_t* w, bool full_warp, bool valid, int lane, int64_t row,
                                          int col, int row_base) {
+    constexpr int CHUNKS = BOXW / 8;  // 16-byte chunks per row
     if (STAGED && full_warp) {
-        const uint32_t stg = stg_base + (uint32_t)((nbox % NBUF) * STG_BYTES);
+        const uint32_t stg = stg_base + (uint32_t)((nbox % NBUF) * (32 * BOXW * 2));
         ++nbox;
-        if (lane == 0) {  // the store that last used this box has read it
+        if (TMA_STORE && lane == 0) {  // the store that last used this box has read it
             if (NBUF == 2) bulk_wait_read_1(); else bulk_wait_read();
         }
         __syncwarp();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const uint32_t a = stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4);
+        for (int c = 0; c < CHUNKS; ++c) {
+            const int sw = CHUNKS == 4 ? ((lane >> 1) & 3) : (lane & 7);  // the 64B / 128B swizzle
+            const uint32_t a = stg + lane * (BOXW * 2) + ((c ^ sw) << 4);
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
                          :: "r"(a), "r"(w[4 * c]), "r"(w[4 * c + 1]), "r"(w[4 * c + 2]), "r"(w[4 * c + 3])
                          : "memory");
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-            tma_store_2d(tmO, stg, col, row_base);
-            bulk_commit();
+        if (TMA_STORE) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_2d(tmO, stg, col, row_base);
+                bulk_commit();
+            }
+        } else {
+            // read back row-major: each instruction moves 32 x 16 bytes of whole
+            // consecutive rows (full 128-byte lines at BOXW = 64), so the
+            // stores leave the SM coalesced without occupying the TMA unit
+            __syncwarp();
+            constexpr int RPI = 32 / CHUNKS;  // rows per instruction
+            const int rr = lane / CHUNKS, c = lane % CHUNKS;
+#pragma unroll
+            for (int i = 0; i < 32 / RPI; ++i) {
+                const int r = i * RPI + rr;
+                const int sw = CHUNKS == 4 ? ((r >> 1) & 3) : (r & 7);
+                uint4 v;
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                             : "r"(stg + r * (BOXW * 2) + ((c ^ sw) << 4)) : "memory");
+                *reinterpret_cast<uint4*>(p.out + (int64_t)(row_base + r) * p.ldo + col + c * 8) = v;
+            }
+            __syncwarp();  // the box is read before the warp's next box overwrites it
         }
     } else if (valid) {
         uint4* dst = reinterpret_cast<uint4*>(p.out + row * p.ldo + col);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) dst[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+        for (int c = 0; c < CHUNKS; ++c) dst[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
     }
 }
 
@@ -300,6 +338,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     constexpr int STAGES = C::STAGES, A_BYTES = C::A_BYTES, B_BYTES = C::B_BYTES, ATOMS = C::ATOMS;
     constexpr int SFB_BYTES = C::SFB_BYTES, ROWB = C::ROWB, SWZ = C::SWZ, SBO = C::SBO;
     constexpr uint32_t SF_STAGE_COLS = C::SF_STAGE_COLS;
+    constexpr int TN = C::TN, ACC_BUFS = C::ACC_BUFS, SFB_BLOCKS = C::SFB_BLOCKS, B_ROWS = C::B_ROWS;
     extern __shared__ uint8_t smem_raw[];
     Smem<MODE>& s = *reinterpret_cast<Smem<MODE>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -323,9 +362,12 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             mbar_init(smem_u32(&s.sf_full[i]), 8);
             mbar_init(smem_u32(&s.empty[i]), 1);
         }
-        mbar_init(smem_u32(&s.tmem_full), 1);
-        mbar_init(smem_u32(&s.tmem_empty), 2);
-        mbar_init(smem_u32(&s.epi_done), EPI_WARPS);
+        for (int i = 0; i < ACC_BUFS; ++i) {
+            mbar_init(smem_u32(&s.tmem_full[i]), 1);
+            mbar_init(smem_u32(&s.tmem_empty[i]), 2);
+            // per accumulator: a warp's arrival for tile t + ACC_BUFS waits for tile t's release
+            mbar_init(smem_u32(&s.epi_done[i]), EPI_WARPS);
+        }
         mbar_init(smem_u32(&s.drain), 1);
         s.abort = 0;
         fence_barrier_init();
@@ -363,7 +405,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const uint32_t tmem = s.tmem_base;
     volatile int* abort = &s.abort;
 
-    const int n_tiles = MODE == 1 ? p.N / 256 : p.N / BN;  // mode 1: 128 gate + 128 up columns per tile
+    const int n_tiles = p.N / TN;  // mode 1: 128 gate + 128 up columns per tile
     const int total = s.ppre[G] * n_tiles;
     const int k_atoms = p.K / 64;
     const int k_stages = (k_atoms + ATOMS - 1) / ATOMS;
@@ -379,11 +421,12 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             bool ok = true;
             for (int u = pair; u < total && ok; u += n_pairs) {
                 const Tile x = decode_unit(s, G, n_tiles, u, rank);
-                // 128-row weight blocks of the pair's two halves: mode 1 takes
-                // 128 gate and 128 up rows of the expert, mode 0 two adjacent blocks
-                const int jb0 = MODE == 1 ? x.g * (p.N / 128) + x.nt : x.g * (p.N / 128) + 2 * x.nt;
-                const int jb1 = MODE == 1 ? x.g * (p.N / 128) + p.N / 256 + x.nt : jb0 + 1;
-                const int jb = rank == 0 ? jb0 : jb1;
+                // 128-row weight blocks of the tile: mode 1 takes 128 gate and
+                // 128 up rows of the expert (one per CTA), mode 0 the tile's
+                // SFB_BLOCKS adjacent blocks, each CTA staging half the rows
+                const int jb0 = x.g * (p.N / 128) + (MODE == 1 ? 1 : SFB_BLOCKS) * x.nt;
+                const int jb1 = x.g * (p.N / 128) + p.N / 256 + x.nt;
+                const int brow = MODE == 1 ? (rank == 0 ? jb0 : jb1) * 128 : jb0 * 128 + (int)rank * B_ROWS;
                 for (int ks = 0; ks < k_stages; ++ks) {
                     if (!mbar_wait_bounded(smem_u32(&s.empty[stage]), phase ^ 1, abort, p.err)) { ok = false; break; }
                     const uint32_t fb = smem_u32(&full[stage]);
@@ -396,7 +439,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     } else {
                         // the scale box is always whole: atoms past K are zero-filled
                         mbar_arrive_expect_tx(fb, B_BYTES + SFB_BYTES);
-                        tma_load_2d(smem_u32(s.b[stage]), &tmB, fb, ks * ROWB, jb * 128);
+                        tma_load_2d(smem_u32(s.b[stage]), &tmB, fb, ks * ROWB, brow);
                         if (MODE == 1)
                             tma_load_4d(smem_u32(s.sfb[stage]), &tmSFB, fb, 0, ks * ATOMS, x.nt, 2 * x.g);
                         else
@@ -427,11 +470,14 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             // after the peer's have.
             const uint64_t adesc0 = smem_desc(smem_u32(s.a[0]), 0, SBO, SWZ);
             const uint64_t bdesc0 = smem_desc(smem_u32(s.b[0]), 0, SBO, SWZ);
-            int stage = 0;
-            uint32_t phase = 0, acc_phase = 0;
+            int stage = 0, it = 0;
+            uint32_t phase = 0;
             bool ok = true;
-            for (int u = pair; u < total && ok; u += n_pairs) {
-                if (!mbar_wait_bounded_relaxed(smem_u32(&s.tmem_empty), acc_phase ^ 1, abort, p.err)) { ok = false; break; }
+            for (int u = pair; u < total && ok; u += n_pairs, ++it) {
+                // accumulator it % ACC_BUFS, in its (it / ACC_BUFS)-th use
+                const int ab = ACC_BUFS == 1 ? 0 : (it & 1);
+                const uint32_t acc_phase = (uint32_t)(ACC_BUFS == 1 ? it : it >> 1) & 1u;
+                if (!mbar_wait_bounded_relaxed(smem_u32(&s.tmem_empty[ab]), acc_phase ^ 1, abort, p.err)) { ok = false; break; }
                 tc_fence_after();
                 for (int ks = 0; ks < k_stages; ++ks) {
                     if (!mbar_wait_bounded_relaxed(smem_u32(&s.sf_full[stage]), phase, abort, p.err)) { ok = false; break; }
@@ -443,15 +489,14 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 #pragma unroll
                     for (int kk = 0; kk < ATOMS; ++kk) {
                         if (kk < na)
-                            tc_mma2_nvfp4(tmem + ACC_COL, ad + 2 * kk, bd + 2 * kk, IDESC, sfc + kk * 4,
-                                          sfc + 4 * ATOMS + kk * 8, (ks | kk) != 0);
+                            tc_mma2_nvfp4(tmem + ACC_COL + ab * TN, ad + 2 * kk, bd + 2 * kk, C::IDESC, sfc + kk * 4,
+                                          sfc + 4 * ATOMS + kk * 4 * SFB_BLOCKS, (ks | kk) != 0);
                     }
                     tc_commit2_mc(smem_u32(&s.empty[stage]), 3);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
-                tc_commit2_mc(smem_u32(&s.tmem_full), 3);
-                acc_phase ^= 1;
+                tc_commit2_mc(smem_u32(&s.tmem_full[ab]), 3);
             }
             if (!ok) raise_abort(&s.abort, rank);
             // every MMA issued by this thread completes before TMEM is released
@@ -464,7 +509,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         // of 16 bytes; line i holds the 4 scales of rows i, i+32, i+64, i+96)
         // goes to 4 consecutive columns of every quarter: thread i of each
         // quarter writes line i.  SFA atom kk -> columns sfc + 4kk; SFB atom kk
-        // of half hh -> columns sfc + 4*ATOMS + 8kk + 4hh.
+        // of 128-row block hh -> columns sfc + 4*ATOMS + 4*SFB_BLOCKS*kk + 4hh.
         const int q = warp & 3;
         const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
         int stage = 0;
@@ -478,11 +523,13 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 #pragma unroll
                 for (int kk = 0; kk < ATOMS; ++kk) {
                     const uint4 a = *reinterpret_cast<const uint4*>(s.sfa[stage] + kk * 512 + lane * 16);
-                    const uint4 b0 = *reinterpret_cast<const uint4*>(s.sfb[stage] + kk * 512 + lane * 16);
-                    const uint4 b1 = *reinterpret_cast<const uint4*>(s.sfb[stage] + SFB_BYTES / 2 + kk * 512 + lane * 16);
                     tmem_st4(sfc + kk * 4, a.x, a.y, a.z, a.w);
-                    tmem_st4(sfc + 4 * ATOMS + kk * 8, b0.x, b0.y, b0.z, b0.w);
-                    tmem_st4(sfc + 4 * ATOMS + 4 + kk * 8, b1.x, b1.y, b1.z, b1.w);
+#pragma unroll
+                    for (int hh = 0; hh < SFB_BLOCKS; ++hh) {
+                        const uint4 b = *reinterpret_cast<const uint4*>(s.sfb[stage] + hh * (ATOMS * 512) + kk * 512 +
+                                                                        lane * 16);
+                        tmem_st4(sfc + 4 * ATOMS + kk * 4 * SFB_BLOCKS + 4 * hh, b.x, b.y, b.z, b.w);
+                    }
                 }
                 tmem_st_wait();
                 tc_fence_before();
@@ -494,17 +541,19 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         if (!ok && lane == 0) raise_abort(&s.abort, rank);
     } else if (warp < PRODB_WARP) {
         // ---------------------------------------------------------------- epilogue
-        // Each warp copies its 32 rows x 64 accumulator columns into registers;
-        // once all 16 have, warp 6 releases the CTA's TMEM with one arrival, so
-        // the next tile's MMAs run while the warps scale, activate and store.
+        // Each warp copies its 32 rows x (64 in mode 1, 32 in mode 0)
+        // accumulator columns into registers; once all 16 have, warp 6
+        // releases the CTA's half of that accumulator with one arrival, so the
+        // MMAs that need it can run while the warps scale, activate and store.
         const int q = warp & 3;                    // TMEM lane quarter this warp may access
         const int cg = (warp - EPI_WARP0) >> 2;    // column group 0..3
         const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
-        const uint32_t release = mapa_shared(smem_u32(&s.tmem_empty), 0);
-        uint32_t acc_phase = 0;
         bool ok = true;
         int nbox = 0;  // staged boxes this warp has stored
-        for (int u = pair; u < total; u += n_pairs) {
+        int it = 0;    // tiles of this CTA so far
+        for (int u = pair; u < total; u += n_pairs, ++it) {
+            const int ab = ACC_BUFS == 1 ? 0 : (it & 1);
+            const uint32_t acc_phase = (uint32_t)(ACC_BUFS == 1 ? it : it >> 1) & 1u;
             const Tile x = decode_unit(s, G, n_tiles, u, rank);
             const int rl = q * 32 + lane;
             const bool valid = rl < x.rows;
@@ -513,12 +562,12 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             const float sa = valid ? __ldg(p.a_scale + row) : 0.0f;
             const float sbw = __ldg(p.b_scale + x.g);
             const float prob = (valid && p.row_prob) ? __ldg(p.row_prob + row) : 1.0f;
-            if (!mbar_wait_bounded_relaxed(smem_u32(&s.tmem_full), acc_phase, abort, p.err)) { ok = false; break; }
+            if (!mbar_wait_bounded_relaxed(smem_u32(&s.tmem_full[ab]), acc_phase, abort, p.err)) { ok = false; break; }
             tc_fence_after();
-            uint32_t v[64];
+            uint32_t v[MODE == 0 ? C::BOXW : 64];
             if (MODE == 0) {
-                tmem_ld32(lane_addr + ACC_COL + cg * 64, v);
-                tmem_ld32(lane_addr + ACC_COL + cg * 64 + 32, v + 32);
+#pragma unroll
+                for (int h = 0; h < C::BOXW / 32; ++h) tmem_ld32(lane_addr + ACC_COL + ab * TN + cg * C::BOXW + 32 * h, v + 32 * h);
             } else {
                 tmem_ld32(lane_addr + ACC_COL + cg * 32, v);             // gate
                 tmem_ld32(lane_addr + ACC_COL + 128 + cg * 32, v + 32);  // up
@@ -526,12 +575,12 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&s.epi_done));
+            if (lane == 0) mbar_arrive(smem_u32(&s.epi_done[ab]));
             if (warp == EPI_WARP0) {
                 if (lane == 0) {
-                    if (mbar_wait_bounded(smem_u32(&s.epi_done), acc_phase, abort, p.err)) {
+                    if (mbar_wait_bounded(smem_u32(&s.epi_done[ab]), acc_phase, abort, p.err)) {
                         tc_fence_after();
-                        mbar_arrive_cluster(release);
+                        mbar_arrive_cluster(mapa_shared(smem_u32(&s.tmem_empty[ab]), 0));
                     } else {
                         ok = false;
                     }
@@ -539,7 +588,6 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) break;
             }
-            acc_phase ^= 1;
             if (x.rows == 0) continue;  // the odd CTA of a group's last pair: nothing to store
             const float scale = __fmul_rn(sa, sbw);
             const uint64_t scale2 = f2(scale, scale);
@@ -547,14 +595,12 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             const bool full_warp = q * 32 + 32 <= x.rows;
             const uint32_t stg = smem_u32(s.stg[(warp - EPI_WARP0) * C::NBUF]);
             if (MODE == 0) {
-                uint32_t w[32];  // convert all 64 values first: the fp32 registers die as they are packed
+                uint32_t w[C::BOXW / 2];
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
+                for (int j = 0; j < C::BOXW / 2; ++j)
                     w[j] = pack_bf16x2(f2_mul(f2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), scale2));
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf)
-                    emit_box<C::STAGED, C::NBUF>(p, &tmO, stg, nbox, w + hf * 16, full_warp, valid, lane, row,
-                                                 x.nt * BN + cg * 64 + hf * 32, x.row0 + q * 32);
+                emit_box<C::STAGED, C::NBUF, C::BOXW, C::TMA_STORE>(p, &tmO, stg, nbox, w, full_warp, valid, lane, row,
+                                                      x.nt * TN + cg * C::BOXW, x.row0 + q * 32);
             } else {
                 if (valid && p.c_debug) {
                     float* cgp = p.c_debug + row * p.N + x.nt * 128 + cg * 32;
@@ -574,8 +620,8 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 const uint64_t escale2 = f2(es, es);
                 uint32_t mw = p.row_prob ? swiglu_words<true>(v, scale2, escale2, f2(prob, prob), w)
                                          : swiglu_words<false>(v, scale2, escale2, 0, w);
-                emit_box<C::STAGED, C::NBUF>(p, &tmO, stg, nbox, w, full_warp, valid, lane, row, x.nt * 128 + cg * 32,
-                                             x.row0 + q * 32);
+                emit_box<C::STAGED, C::NBUF, C::BOXW, C::TMA_STORE>(p, &tmO, stg, nbox, w, full_warp, valid, lane, row,
+                                                      x.nt * 128 + cg * 32, x.row0 + q * 32);
                 // the row's max |bf16(d)| over this warp's 32 columns
                 if (valid) {
                     mw = __vmaxu2(mw, mw >> 16);
@@ -619,14 +665,14 @@ EncodeTiledFn encode_fn() {
 }
 
 // 2D uint8 view [rows x row_bytes] of packed FP4 codes: boxes of ROWB bytes x
-// 128 rows, swizzled to match the MMA descriptors of the mode.
-bool make_codes_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes, int mode) {
+// box_rows rows, swizzled to match the MMA descriptors of the mode.
+bool make_codes_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes, int mode, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const int rowb = mode == 0 ? Cfg<0>::ROWB : Cfg<1>::ROWB;
     cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-    cuuint32_t box[2] = {(cuuint32_t)rowb, 128};
+    cuuint32_t box[2] = {(cuuint32_t)rowb, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, rowb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
@@ -634,11 +680,11 @@ bool make_codes_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_
 }
 
 // Weight scales, stored as 128-row blocks of k_atoms 512-byte atoms, viewed
-// as 32-bit words so one tensor copy brings a stage's atoms of the pair's two
-// 128-row blocks: mode 0 (adjacent blocks jb, jb + 1) as 3D {128, k_atoms,
-// G*N/128} with box {128, ATOMS, 2}; mode 1 (gate block nt and up block
-// N/256 + nt of expert g) as 4D {128, k_atoms, N/256, 2G} with box {128,
-// ATOMS, 1, 2}, the up block being one step of the last dimension away.
+// as 32-bit words so one tensor copy brings a stage's atoms of the tile's
+// weight rows: mode 0 (the tile's blocks from jb) as 3D {128, k_atoms, G*N/128}
+// with box {128, ATOMS, blocks per tile}; mode 1 (gate block nt and up block N/256 + nt of expert
+// g) as 4D {128, k_atoms, N/256, 2G} with box {128, ATOMS, 1, 2}, the up
+// block being one step of the last dimension away.
 bool make_sfb_map(CUtensorMap* m, const void* base, int G, int N, int K, int mode) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
@@ -648,7 +694,7 @@ bool make_sfb_map(CUtensorMap* m, const void* base, int G, int N, int K, int mod
     if (mode == 0) {
         cuuint64_t dims[3] = {128, k_atoms, (cuuint64_t)G * (N / 128)};
         cuuint64_t strides[2] = {512, k_atoms * 512};
-        cuuint32_t box[3] = {128, atoms, 2};
+        cuuint32_t box[3] = {128, atoms, (cuuint32_t)Cfg<0>::SFB_BLOCKS};
         return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -661,16 +707,18 @@ bool make_sfb_map(CUtensorMap* m, const void* base, int G, int N, int K, int mod
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2D bf16 view [rows x cols] (row stride ld elements) of an output, 32 x 32 boxes, 64B swizzle.
-bool make_out_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld) {
+// 2D bf16 view [rows x cols] (row stride ld elements) of an output: 32-row
+// boxes of box_cols columns, 64B swizzle for 32 columns, 128B for 64.
+bool make_out_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_cols) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
-    cuuint32_t box[2] = {32, 32};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, 32};
     cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -740,11 +788,13 @@ int device_sm_count() {
 cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
     if (g.M <= 0) return cudaSuccess;
     CUtensorMap ta, tb, tsfb, to;
-    if (!make_codes_map(&ta, g.a_codes, g.M, g.K / 2, g.mode)) return cudaErrorInvalidValue;
-    if (!make_codes_map(&tb, g.b_codes, (int64_t)g.G * g.N, g.K / 2, g.mode)) return cudaErrorInvalidValue;
+    if (!make_codes_map(&ta, g.a_codes, g.M, g.K / 2, g.mode, BM)) return cudaErrorInvalidValue;
+    const int b_rows = g.mode == 0 ? Cfg<0>::B_ROWS : Cfg<1>::B_ROWS;
+    if (!make_codes_map(&tb, g.b_codes, (int64_t)g.G * g.N, g.K / 2, g.mode, b_rows)) return cudaErrorInvalidValue;
     if (!make_sfb_map(&tsfb, g.b_sf, g.goff ? g.G : 1, g.N, g.K, g.mode)) return cudaErrorInvalidValue;
     const int64_t out_cols = g.mode == 1 ? g.N / 2 : g.N;
-    if (!make_out_map(&to, g.out, g.M, out_cols, g.ldo)) return cudaErrorInvalidValue;
+    const int box_cols = g.mode == 0 ? Cfg<0>::BOXW : Cfg<1>::BOXW;
+    if (!make_out_map(&to, g.out, g.M, out_cols, g.ldo, box_cols)) return cudaErrorInvalidValue;
     KParams p;
     p.a_sf = g.a_sf;
     p.a_scale = g.a_scale;
@@ -765,7 +815,8 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
     p.err = g.err;
     const int num_sms = g.num_sms > 0 ? g.num_sms : 148;
     // dense calls: no more pairs than units of work (m-tile pairs x n-tiles)
-    const int64_t dense_units = g.goff == nullptr ? ((g.M + BM - 1) / BM + 1) / 2 * (g.N / BN) : 0;
+    const int tn = g.mode == 0 ? Cfg<0>::TN : Cfg<1>::TN;
+    const int64_t dense_units = g.goff == nullptr ? ((g.M + BM - 1) / BM + 1) / 2 * (g.N / tn) : 0;
     if (g.mode == 0) return launch_mode<0>(ta, tb, tsfb, to, p, num_sms, dense_units, stream);
     return launch_mode<1>(ta, tb, tsfb, to, p, num_sms, dense_units, stream);
 }
