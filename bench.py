@@ -68,8 +68,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--quick", action="store_true", help="profiling runs: no e2e, no oracle, no clocks")
-    p.add_argument("--only", choices=["all", "quant"], default="all",
-                   help="quant: time only the 16384 x 2048 quantizer workload (for profiling)")
+    p.add_argument("--only", choices=["all", "quant", "dequant"], default="all",
+                   help="quant / dequant: time only the 16384 x 2048 quantizer / dequantizer workload (for profiling)")
     return p.parse_args()
 
 
@@ -401,6 +401,42 @@ def quant_gbs(args, local, reps=50, four_over_six=None):
     return out
 
 
+def dequant_gbs(args, local, reps=50):
+    """DQ(Q(x)) throughput: the 16384 x 2048 workload quantized once, then
+    dequantized to bf16 per rep (L2 flushed per rep)."""
+    import nvfp4_quantized_moe_token_gb300 as nv
+    dev = torch.device("cuda", local)
+    xb = workloads.quant_rows()["x"]
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).to(dev)
+    q = nv.quantize_rows(x)
+    y = torch.empty_like(x)
+    flush = L2Flush(dev)
+    for _ in range(5):
+        nv.dequantize_rows(q, out=y)
+    ts = []
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("timed_dequant")
+    for _ in range(reps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        nv.dequantize_rows(q, out=y)
+        b.record()
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
+    ms = statistics.fmean(a.elapsed_time(b) for a, b in ts)
+    nbytes = 16384 * (1024 + 128 + 4 + 2048 * 2)  # codes, scales, row scale in; bf16 out
+    hbm = 6800.0
+    pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk):
+        with open(pk) as f:
+            hbm = json.load(f).get("hbm_gbs", hbm)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"workload": "dequantize (DQ(Q(x)) -> bf16) 16384 x 2048", "us": ms * 1e3, "gbs": gbs,
+            "algorithmic_bytes": nbytes, "frac_of_hbm": gbs / hbm, "hbm_peak_gbs": hbm}
+
+
 # ---------------------------------------------------------------- oracle timing
 
 def oracle_setup(d):
@@ -477,15 +513,17 @@ def main():
         return
     import nvfp4_quantized_moe_token_gb300 as nv
     nv.lib()
-    if args.only == "quant":
+    if args.only in ("quant", "dequant"):
         if rank == 0:
-            print(json.dumps({"quant": quant_gbs(args, local, reps=max(args.steps, 1))}))
+            fn = quant_gbs if args.only == "quant" else dequant_gbs
+            print(json.dumps({args.only: fn(args, local, reps=max(args.steps, 1))}))
         return
     res, d = run_ours(args, rank, world, local)
     if rank == 0:
         if not args.quick:
             res["quant"] = quant_gbs(args, local)
             res["quant_four_over_six"] = quant_gbs(args, local, four_over_six="mse")
+            res["dequant"] = dequant_gbs(args, local)
         if not (args.no_cpu_baseline or args.quick):
             res["cpu_baseline"] = cpu_baseline(d)
         print(json.dumps(res))

@@ -150,6 +150,30 @@ NVFP4_API int nvfp4_quantize_rows(const void* x_bf16, int64_t rows, int64_t cols
                         void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * nvfp4_dequantize_rows: y[r][j] = bf16(q[r][j] * s_b[r][j/16] * s_g) for an
+ * NVFP4 matrix `in` [rows x cols] as nvfp4_quantize_rows writes it (swizzled
+ * block scales), rounded once to nearest even from the exact product.  This
+ * is DQ(Q(x)), the BF16 backward operand that keeps the forward pass's
+ * quantization decisions (the pages' "Improving Gradient Stability":
+ * dequantized backward for weights and activations; decode as "miniTE
+ * Technical Report" 2.2).  s_g = in->scale[r] (NVFP4_PER_ROW) or
+ * in->scale[0] (NVFP4_PER_TENSOR); four-over-six flags are ignored (the
+ * decode rule is the same).
+ * group_offsets / padded_offsets (nullable, device, [groups + 1]): the block
+ * scales of row r live at padded row padded_offsets[g] + (r -
+ * group_offsets[g]) for the group g holding r, as in the expert-ordered
+ * buffers of moe_expert_forward (a1, a2); NULL = scale row r.
+ * y is bf16 [rows x cols], row stride ldy elements.
+ * Shapes: rows >= 0, 0 < cols <= 32768, cols % 16 == 0, ldy >= cols,
+ *         ldy % 8 == 0; 1 <= groups <= 256 when offsets are given.
+ *         rows == 0 is a no-op (the buffers may then be null).
+ * Alignment: codes 16-byte aligned, y 16-byte aligned, scale 4-byte aligned.
+ */
+NVFP4_API int nvfp4_dequantize_rows(const nvfp4_tensor* in, int scale_mode, const int* group_offsets,
+                                    const int* padded_offsets, int groups, void* y_bf16, int64_t ldy,
+                                    void* stream);
+
+/*
  * nvfp4_linear: y[m][n] = bf16( s_gx[m] * s_gw * sum_k (q_x s_bx)(q_w s_bw) )
  * for x [M x K] quantized per row and w [N x K] (K-major, i.e. the weight
  * transposed) quantized per tensor.  Accumulation is fp32 on the tensor

@@ -47,7 +47,8 @@ class _Layout(ctypes.Structure):
 PER_ROW = 0
 PER_TENSOR = 1
 FOUR_OVER_SIX = {None: 0, "mse": 2, "mae": 4}  # scale-mode flags of four-over-six block scaling
-SYMBOLS = ["nvfp4_sf_bytes", "nvfp4_quantize_workspace", "nvfp4_quantize_rows", "nvfp4_linear",
+SYMBOLS = ["nvfp4_sf_bytes", "nvfp4_quantize_workspace", "nvfp4_quantize_rows", "nvfp4_dequantize_rows",
+           "nvfp4_linear",
            "moe_expert_workspace_layout", "moe_expert_workspace", "moe_expert_forward",
            "moe_expert_forward_noalloc", "nvfp4_last_error"]
 
@@ -76,6 +77,9 @@ def lib():
         L.nvfp4_quantize_rows.restype = ctypes.c_int
         L.nvfp4_quantize_rows.argtypes = [c_vp, c_i64, c_i64, c_i64, ctypes.c_int, c_vp,
                                           ctypes.POINTER(_Tensor), c_vp, ctypes.c_size_t, c_vp]
+        L.nvfp4_dequantize_rows.restype = ctypes.c_int
+        L.nvfp4_dequantize_rows.argtypes = [ctypes.POINTER(_Tensor), ctypes.c_int, c_vp, c_vp, ctypes.c_int, c_vp,
+                                            c_i64, c_vp]
         L.nvfp4_linear.restype = ctypes.c_int
         L.nvfp4_linear.argtypes = [ctypes.POINTER(_Tensor), ctypes.POINTER(_Tensor), c_vp, c_i64,
                                    c_vp, ctypes.c_size_t, c_vp]
@@ -149,6 +153,22 @@ def quantize_rows(x, per_tensor=False, amax_in=None, out=None, four_over_six=Non
     rc = lib().nvfp4_quantize_rows(_ptr(x), rows, cols, x.stride(0), mode, _ptr(amax_in), ctypes.byref(t),
                                    _ptr(ws), ws_bytes, _stream(stream))
     _check(rc, "nvfp4_quantize_rows")
+    return out
+
+
+def dequantize_rows(t, per_tensor=False, group_offsets=None, padded_offsets=None, out=None, stream=None):
+    """NVFP4Tensor -> bf16 [rows, cols] = bf16(q s_b s_g), the exact product rounded
+    once (DQ(Q(x)), the BF16 backward operand).  group_offsets / padded_offsets
+    (int32 CUDA tensors [G+1]): scale rows padded per group, as in the expert-ordered
+    buffers of moe_expert_forward."""
+    if out is None:
+        out = torch.empty((t.rows, t.cols), dtype=torch.bfloat16, device=t.codes.device)
+    assert out.dtype == torch.bfloat16 and out.stride(1) == 1
+    G = 0 if group_offsets is None else group_offsets.numel() - 1
+    rc = lib().nvfp4_dequantize_rows(ctypes.byref(t.c()), PER_TENSOR if per_tensor else PER_ROW,
+                                     _ptr(group_offsets), _ptr(padded_offsets), G, _ptr(out), out.stride(0),
+                                     _stream(stream))
+    _check(rc, "nvfp4_dequantize_rows")
     return out
 
 

@@ -122,6 +122,40 @@ int nvfp4_quantize_rows(const void* x_bf16, int64_t rows, int64_t cols, int64_t 
     return ok();
 }
 
+int nvfp4_dequantize_rows(const nvfp4_tensor* in, int scale_mode, const int* group_offsets,
+                          const int* padded_offsets, int groups, void* y_bf16, int64_t ldy, void* stream) {
+    if (in != nullptr && in->rows == 0 && in->cols > 0 && in->cols % 16 == 0) return ok();  // nothing to write
+    int rc = check_tensor(in, "dequantize in");
+    if (rc) return rc;
+    if (y_bf16 == nullptr) return fail(NVFP4_EINVAL, "dequantize: y is null");
+    if (!fos_flags_valid(scale_mode & ~NVFP4_PER_TENSOR))
+        return fail(NVFP4_EINVAL, "dequantize: unknown scale_mode %d", scale_mode);
+    const int64_t rows = in->rows, cols = in->cols;
+    if (cols % 16 != 0) return fail(NVFP4_ESHAPE, "dequantize: cols %% 16 != 0 (cols = %lld)", (long long)cols);
+    if (rows >= (1ll << 31) || cols > 32768) return fail(NVFP4_ESHAPE, "dequantize: rows >= 2^31 or cols > 32768");
+    if (ldy < cols || ldy % 8 != 0) return fail(NVFP4_EALIGN, "dequantize: ldy must be >= cols and a multiple of 8");
+    if (!aligned(y_bf16, 16)) return fail(NVFP4_EALIGN, "dequantize: y must be 16-byte aligned");
+    if ((group_offsets == nullptr) != (padded_offsets == nullptr))
+        return fail(NVFP4_EINVAL, "dequantize: group_offsets and padded_offsets go together");
+    if (group_offsets != nullptr && (groups < 1 || groups > 256))
+        return fail(NVFP4_ESHAPE, "dequantize: groups must be in [1, 256]");
+    nvfp4::DequantLaunch d{};
+    d.codes = in->codes;
+    d.sf = in->sf;
+    d.scale = in->scale;
+    d.rows = rows;
+    d.cols = cols;
+    d.per_tensor = (scale_mode & NVFP4_PER_TENSOR) != 0;
+    d.goff = group_offsets;
+    d.gpoff = padded_offsets;
+    d.G = group_offsets != nullptr ? groups : 0;
+    d.y = y_bf16;
+    d.ldy = ldy;
+    cudaError_t e = nvfp4::launch_dequantize(d, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(NVFP4_ELAUNCH, "dequantize: %s", cudaGetErrorString(e));
+    return ok();
+}
+
 int nvfp4_linear(const nvfp4_tensor* x, const nvfp4_tensor* w, void* y_bf16, int64_t ldy, void* ws,
                  size_t ws_bytes, void* stream) {
     int rc = check_tensor(x, "linear x");

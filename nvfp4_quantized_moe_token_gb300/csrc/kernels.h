@@ -26,6 +26,21 @@ struct QuantLaunch {
 };
 cudaError_t launch_quantize(const QuantLaunch& q, cudaStream_t stream);
 
+// NVFP4 rows -> bf16 y = RN16(q s_b s_g) (the exact product, rounded once).
+struct DequantLaunch {
+    const uint8_t* codes;   // [rows x cols/2]
+    const uint8_t* sf;      // swizzled block scales
+    const float* scale;     // [rows], or [1] when per_tensor
+    int64_t rows, cols;
+    int per_tensor;
+    const int* goff;        // nullable: scale rows padded per group (goff/gpoff [G+1])
+    const int* gpoff;
+    int G;
+    void* y;                // bf16, row stride ldy elements
+    int64_t ldy;
+};
+cudaError_t launch_dequantize(const DequantLaunch& d, cudaStream_t stream);
+
 // Grouped / dense block-scaled NVFP4 GEMM on tcgen05.
 //   A rows [M_total x K] (codes + swizzled scales padded per group by
 //   gpoff + per-row fp32 scale); B per group [N x K] (codes + swizzled

@@ -174,6 +174,15 @@ def dequantize(codes, sf_lin, scale, per_tensor=False):
     return out
 
 
+def dequantize_bf16(codes, sf_lin, scale, per_tensor=False):
+    """DQ(Q(x)): the BF16-dequantized value of the exact quantized tensor, the
+    operand of the dequantized backward ("Per-token NVFP4 and Dequantized
+    Backward", Improving Gradient Stability).  The exact value q s_b s_g
+    (decode of "miniTE Technical Report" 2.2; at most 30 significant bits, so
+    exact in fp64) rounded once to bf16, nearest even.  Returns uint16 bits."""
+    return bf16_round(dequantize(codes, sf_lin, scale, per_tensor))
+
+
 def sf_offset(r, c, sf_cols):
     return int(lib().orc_sf_offset(int(r), int(c), int(sf_cols)))
 
