@@ -204,8 +204,9 @@ typedef struct moe_debug {
     /* fp32 [R x 2F], R = T*topk rows in expert order: the FC1 output after
      * the alpha scaling, before SwiGLU (gate columns then up columns). */
     float* fc1_out;
-    /* MOE_STAGE_EVENTS cudaEvent_t handles (created by the caller) recorded
-     * on `stream` before the first stage and after each stage: quantize X
+    /* MOE_STAGE_EVENTS cudaEvent_t handles (created by the caller; a NULL
+     * entry is skipped) recorded on `stream` before the first stage and after
+     * each stage: quantize X
      * (with the router top-k, launched together), routing metadata +
      * permute, FC1, requant, FC2, combine. */
     void** stage_events;

@@ -215,8 +215,9 @@ def moe_expert_forward(x, logits, bias, w1q, w2q, F, topk, weight_at_fc1=False, 
     """One W4A4 MoE expert layer on the device.  Returns (out bf16 [T, H], ws).
     four_over_six (None, 'mse', 'mae'): four-over-six scaling of the activations.
 
-    stage_events (optional): len(STAGES) + 1 torch.cuda.Event objects recorded on
-    the stream before the first stage and after each stage."""
+    stage_events (optional): len(STAGES) + 1 torch.cuda.Event objects (or None
+    for an event to skip) recorded on the stream before the first stage and
+    after each stage."""
     T, H = x.shape
     E = logits.shape[1]
     need = int(lib().moe_expert_workspace(T, H, F, E, topk))
@@ -231,9 +232,9 @@ def moe_expert_forward(x, logits, bias, w1q, w2q, F, topk, weight_at_fc1=False, 
         assert len(stage_events) == len(STAGES) + 1
         st = stream if stream is not None else torch.cuda.current_stream()
         for e in stage_events:
-            if e.cuda_event == 0:  # torch creates the CUDA event on its first record
+            if e is not None and e.cuda_event == 0:  # torch creates the CUDA event on its first record
                 e.record(st)
-        evs = (c_vp * len(stage_events))(*[e.cuda_event for e in stage_events])
+        evs = (c_vp * len(stage_events))(*[None if e is None else e.cuda_event for e in stage_events])
     dbg = _Debug(None if fc1_debug is None else fc1_debug.data_ptr(), evs)
     rc = lib().moe_expert_forward(_ptr(x), T, H, _ptr(logits), _ptr(bias), E, topk, ctypes.byref(a),
                                   ctypes.byref(b), F, ctypes.byref(opt), _ptr(out), ctypes.byref(dbg),

@@ -290,7 +290,8 @@ int moe_expert_forward(const void* x_bf16, int64_t T, int64_t H, const float* ro
     int ev_i = 0;
     auto mark = [&]() -> cudaError_t {
         if (ev == nullptr) return cudaSuccess;
-        return cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[ev_i++]), s);
+        void* e = ev[ev_i++];
+        return e == nullptr ? cudaSuccess : cudaEventRecord(reinterpret_cast<cudaEvent_t>(e), s);
     };
     if ((e = mark()) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe event: %s", cudaGetErrorString(e));
 
