@@ -520,17 +520,25 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 if (!mbar_wait_bounded(smem_u32(&s.full_a[stage]), phase, abort, p.err) ||
                     !mbar_wait_bounded(smem_u32(&s.full_b[stage]), phase, abort, p.err)) { ok = false; break; }
                 const uint32_t sfc = lane_addr + SF_COL + stage * SF_STAGE_COLS;
+                // the stage's SFA columns (4 per atom) and SFB columns (4 per atom and 128-row
+                // block) are contiguous runs: one wide store each
+                uint32_t fa[4 * ATOMS], fb[4 * ATOMS * SFB_BLOCKS];
 #pragma unroll
                 for (int kk = 0; kk < ATOMS; ++kk) {
                     const uint4 a = *reinterpret_cast<const uint4*>(s.sfa[stage] + kk * 512 + lane * 16);
-                    tmem_st4(sfc + kk * 4, a.x, a.y, a.z, a.w);
+                    fa[4 * kk] = a.x; fa[4 * kk + 1] = a.y; fa[4 * kk + 2] = a.z; fa[4 * kk + 3] = a.w;
 #pragma unroll
                     for (int hh = 0; hh < SFB_BLOCKS; ++hh) {
                         const uint4 b = *reinterpret_cast<const uint4*>(s.sfb[stage] + hh * (ATOMS * 512) + kk * 512 +
                                                                         lane * 16);
-                        tmem_st4(sfc + 4 * ATOMS + kk * 4 * SFB_BLOCKS + 4 * hh, b.x, b.y, b.z, b.w);
+                        uint32_t* d = fb + 4 * (SFB_BLOCKS * kk + hh);
+                        d[0] = b.x; d[1] = b.y; d[2] = b.z; d[3] = b.w;
                     }
                 }
+                static_assert(4 * ATOMS == 16 && (SFB_BLOCKS == 1 || SFB_BLOCKS == 2), "scale store widths");
+                tmem_st16(sfc, fa);
+                if constexpr (SFB_BLOCKS == 2) tmem_st32(sfc + 4 * ATOMS, fb);
+                else tmem_st16(sfc + 4 * ATOMS, fb);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
