@@ -437,6 +437,41 @@ def dequant_gbs(args, local, reps=50):
             "algorithmic_bytes": nbytes, "frac_of_hbm": gbs / hbm, "hbm_peak_gbs": hbm}
 
 
+def library_fp4_reference(local, reps=20):
+    """The library NVFP4 GEMM (torch._scaled_mm on float4_e2m1fn_x2 operands
+    with E4M3 16-element block scales, bf16 out) on dense problems of the
+    expert layer's two GEMM shapes and at 8192^3: a measured reference for
+    the tensor-core ceiling, not part of the path.  None where torch lacks it."""
+    dev = torch.device("cuda", local)
+    if not hasattr(torch, "float4_e2m1fn_x2"):
+        return None
+    out = {}
+    for name, (M, N, K) in {"fc1_shape_dense": (T * K_TOP, 2 * F, H), "fc2_shape_dense": (T * K_TOP, H, F),
+                            "square_8192": (8192, 8192, 8192)}.items():
+        try:
+            a = torch.randint(0, 256, (M, K // 2), dtype=torch.uint8, device=dev).view(torch.float4_e2m1fn_x2)
+            b = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device=dev).view(torch.float4_e2m1fn_x2)
+            sa = torch.ones((M + 127) // 128 * 128 * ((K // 16 + 3) // 4 * 4), device=dev).to(torch.float8_e4m3fn)
+            sb = torch.ones((N + 127) // 128 * 128 * ((K // 16 + 3) // 4 * 4), device=dev).to(torch.float8_e4m3fn)
+            for _ in range(3):
+                torch._scaled_mm(a, b.t(), sa, sb, out_dtype=torch.bfloat16)
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            s0.record()
+            for _ in range(reps):
+                torch._scaled_mm(a, b.t(), sa, sb, out_dtype=torch.bfloat16)
+            s1.record()
+            torch.cuda.synchronize()
+            ms = s0.elapsed_time(s1) / reps
+            out[name] = {"m": M, "n": N, "k": K, "us": ms * 1e3, "tflops": 2.0 * M * N * K / (ms / 1e3) / 1e12}
+            del a, b, sa, sb
+        except Exception as ex:  # reported, not retried
+            out[name] = {"error": f"{type(ex).__name__}: {str(ex)[:200]}"}
+    torch.cuda.empty_cache()
+    return {"what": "torch._scaled_mm NVFP4 (cuBLASLt), dense, bf16 out, back-to-back (operands stay in L2 "
+                    "only at 8192^3)", "results": out}
+
+
 # ---------------------------------------------------------------- oracle timing
 
 def oracle_setup(d):
@@ -524,6 +559,7 @@ def main():
             res["quant"] = quant_gbs(args, local)
             res["quant_four_over_six"] = quant_gbs(args, local, four_over_six="mse")
             res["dequant"] = dequant_gbs(args, local)
+            res["library_fp4_reference"] = library_fp4_reference(local)
         if not (args.no_cpu_baseline or args.quick):
             res["cpu_baseline"] = cpu_baseline(d)
         print(json.dumps(res))
