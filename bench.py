@@ -437,6 +437,76 @@ def dequant_gbs(args, local, reps=50):
             "algorithmic_bytes": nbytes, "frac_of_hbm": gbs / hbm, "hbm_peak_gbs": hbm}
 
 
+def _timed(fn, reps, flush=None):
+    ts = []
+    for _ in range(reps):
+        if flush is not None:
+            flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.fmean(a.elapsed_time(b) for a, b in ts)
+
+
+def linear_legs(local, bf16_peak, reps=20):
+    """The dense W4A4 linear on the attention projections of the same model
+    (32768 tokens; QKV 2048 -> 5120, o_proj 4096 -> 2048): per-token
+    quantization of the activations plus the block-scaled GEMM, weights
+    pre-quantized per tensor (L2 flushed per rep)."""
+    import nvfp4_quantized_moe_token_gb300 as nv
+    dev = torch.device("cuda", local)
+    d = workloads.attn_proj()
+    flush = L2Flush(dev)
+    out = {}
+    for name, xk, wk in (("qkv_proj", "x", "wqkv"), ("o_proj", "o", "wo")):
+        x = torch.from_numpy(d[xk].view(np.int16)).view(torch.bfloat16).to(dev)
+        w = torch.from_numpy(d[wk].view(np.int16)).view(torch.bfloat16).to(dev)
+        M, K = x.shape
+        N = w.shape[0]
+        wq = nv.quantize_rows(w, per_tensor=True)
+        xq = nv.quantize_rows(x)
+        y = nv.linear(xq, wq)
+        for _ in range(3):
+            nv.quantize_rows(x, out=xq)
+            nv.linear(xq, wq, out=y)
+        torch.cuda.synchronize()
+        q_ms = _timed(lambda: nv.quantize_rows(x, out=xq), reps, flush)
+        g_ms = _timed(lambda: nv.linear(xq, wq, out=y), reps, flush)
+        tf = 2.0 * M * N * K / (g_ms / 1e3) / 1e12
+        peak = bf16_peak * FP4_OVER_BF16
+        out[name] = {"m": M, "n": N, "k": K, "quantize_us": q_ms * 1e3, "gemm_us": g_ms * 1e3,
+                     "step_us": (q_ms + g_ms) * 1e3, "gemm_tflops": tf, "gemm_frac": tf / peak,
+                     "gemm_frac_of_9pf": tf / 9000.0, "quantize_gbs": M * (2 * K + K // 2 + K // 16 + 4) / (q_ms / 1e3) / 1e9}
+        del x, w, xq, wq, y
+    torch.cuda.empty_cache()
+    return {"workload": "attention projections, 32768 tokens, per-token NVFP4 X, per-tensor NVFP4 W",
+            "tokens_per_s_both": 32768 / ((out["qkv_proj"]["step_us"] + out["o_proj"]["step_us"]) / 1e6),
+            "peak_tflops": bf16_peak * FP4_OVER_BF16, **out}
+
+
+def weight_quantize_leg(local):
+    """Per-tensor NVFP4 quantization of the 128 experts' FC1 and FC2 weights
+    (off the timed path of the layer: static weights); bytes read + written."""
+    import nvfp4_quantized_moe_token_gb300 as nv
+    dev = torch.device("cuda", local)
+    d = workloads.moe_32k()
+    w1 = torch.from_numpy(d["w1"].view(np.int16)).view(torch.bfloat16).to(dev)
+    w2 = torch.from_numpy(d["w2"].view(np.int16)).view(torch.bfloat16).to(dev)
+    nv.quantize_grouped_weights(w1)
+    nv.quantize_grouped_weights(w2)
+    torch.cuda.synchronize()
+    ms = _timed(lambda: (nv.quantize_grouped_weights(w1), nv.quantize_grouped_weights(w2)), 3)
+    n = w1.numel() + w2.numel()
+    nbytes = n * 2 * 2 + n // 2 + n // 16  # read twice (tensor amax, then encode), codes + scales written
+    del w1, w2
+    torch.cuda.empty_cache()
+    return {"workload": "128 experts x (W1 1536 x 2048 + W2 2048 x 768), per-tensor scales, 2 x 128 launches pairs",
+            "ms": ms, "gbs": nbytes / (ms / 1e3) / 1e9}
+
+
 def library_fp4_reference(local, reps=20):
     """The library NVFP4 GEMM (torch._scaled_mm on float4_e2m1fn_x2 operands
     with E4M3 16-element block scales, bf16 out) on dense problems of the
@@ -447,6 +517,7 @@ def library_fp4_reference(local, reps=20):
         return None
     out = {}
     for name, (M, N, K) in {"fc1_shape_dense": (T * K_TOP, 2 * F, H), "fc2_shape_dense": (T * K_TOP, H, F),
+                            "qkv_proj": (32768, 5120, 2048), "o_proj": (32768, 2048, 4096),
                             "square_8192": (8192, 8192, 8192)}.items():
         try:
             a = torch.randint(0, 256, (M, K // 2), dtype=torch.uint8, device=dev).view(torch.float4_e2m1fn_x2)
@@ -559,6 +630,8 @@ def main():
             res["quant"] = quant_gbs(args, local)
             res["quant_four_over_six"] = quant_gbs(args, local, four_over_six="mse")
             res["dequant"] = dequant_gbs(args, local)
+            res["linear_attention_projections"] = linear_legs(local, res["roofline"]["peak"] / FP4_OVER_BF16)
+            res["weight_quantize"] = weight_quantize_leg(local)
             res["library_fp4_reference"] = library_fp4_reference(local)
         if not (args.no_cpu_baseline or args.quick):
             res["cpu_baseline"] = cpu_baseline(d)
