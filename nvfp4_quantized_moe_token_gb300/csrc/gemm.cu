@@ -92,6 +92,9 @@ constexpr int MAX_G = 256;
 // rows (0.31 ms), stores from the warps instead of the TMA (coalesced full
 // lines read back from the staging box: 0.38 ms).  The tile shape is a
 // parameter (TN, ACC_BUFS): both forms pass the parity tests.
+// Mode 2 is the plain epilogue for long K loops (K >= 1024, the dense
+// linear): 5 stages in flight, and each warp's 64 columns leave as two
+// 32-column boxes through one staging box (the smem of a fifth stage).
 template <int MODE>
 struct Cfg {
     static constexpr int BK = 256;                      // FP4 elements of K per stage
@@ -100,6 +103,7 @@ struct Cfg {
     static constexpr int ACC_BUFS = 1;                  // accumulators in TMEM (2 fit at TN = 128)
     static constexpr int B_ROWS = TN / 2;               // weight rows staged per CTA (half the tile)
     static constexpr int SFB_BLOCKS = TN / 128;         // 128-row weight-scale blocks per tile
+    static constexpr bool PLAIN = MODE != 1;            // modes 0 and 2: plain bf16 out
     static constexpr int STAGES = MODE == 0 ? 4 : 5;
     static constexpr int NBUF = 1;                      // staging boxes per epilogue warp
     static constexpr int A_BYTES = BM * ROWB;           // this CTA's 128 rows of A
@@ -111,7 +115,8 @@ struct Cfg {
     static constexpr int SBO = 8 * ROWB;                // bytes between 8-row core-matrix groups
     static constexpr uint32_t SF_STAGE_COLS = 4 * ATOMS * (1 + SFB_BLOCKS);  // SFA 4 + SFB 4 per block, per atom
     static constexpr uint32_t IDESC = idesc_nvfp4(2 * BM, TN);
-    static constexpr int BOXW = MODE == 0 ? TN / 4 : 32;  // output columns per epilogue warp = store box width
+    static constexpr int CPW = PLAIN ? TN / 4 : 32;       // output columns per epilogue warp per tile
+    static constexpr int BOXW = MODE == 0 ? CPW : 32;     // store box width (columns)
     static constexpr int STG_BYTES = 32 * BOXW * 2;       // one staging box: 32 rows x BOXW bf16
     static constexpr bool STAGED = true;
     static constexpr bool TMA_STORE = true;               // false: coalesced warp stores from the staging box
@@ -142,9 +147,14 @@ struct __align__(1024) Smem {
     int gpoff[MAX_G + 1];
     int ppre[MAX_G + 1];           // units of m-tile pairs before each group
 };
-static_assert(sizeof(Smem<0>) + 1024 <= 232448 && sizeof(Smem<1>) + 1024 <= 232448, "shared memory per CTA");
+static_assert(sizeof(Smem<0>) + 1024 <= 232448 && sizeof(Smem<1>) + 1024 <= 232448 &&
+              sizeof(Smem<2>) + 1024 <= 232448, "shared memory per CTA");
+// the two plain forms share the host-side tensor maps
+static_assert(Cfg<2>::ROWB == Cfg<0>::ROWB && Cfg<2>::ATOMS == Cfg<0>::ATOMS && Cfg<2>::TN == Cfg<0>::TN &&
+              Cfg<2>::B_ROWS == Cfg<0>::B_ROWS && Cfg<2>::SFB_BLOCKS == Cfg<0>::SFB_BLOCKS, "plain forms");
 // the staging boxes start on 1024-byte boundaries (the TMA swizzle patterns repeat per 1024 bytes)
-static_assert(offsetof(Smem<0>, stg) % 1024 == 0 && offsetof(Smem<1>, stg) % 1024 == 0, "staging alignment");
+static_assert(offsetof(Smem<0>, stg) % 1024 == 0 && offsetof(Smem<1>, stg) % 1024 == 0 &&
+              offsetof(Smem<2>, stg) % 1024 == 0, "staging alignment");
 
 struct KParams {
     const uint8_t* a_sf;
@@ -572,10 +582,10 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             const float prob = (valid && p.row_prob) ? __ldg(p.row_prob + row) : 1.0f;
             if (!mbar_wait_bounded_relaxed(smem_u32(&s.tmem_full[ab]), acc_phase, abort, p.err)) { ok = false; break; }
             tc_fence_after();
-            uint32_t v[MODE == 0 ? C::BOXW : 64];
-            if (MODE == 0) {
+            uint32_t v[C::PLAIN ? C::CPW : 64];
+            if (C::PLAIN) {
 #pragma unroll
-                for (int h = 0; h < C::BOXW / 32; ++h) tmem_ld32(lane_addr + ACC_COL + ab * TN + cg * C::BOXW + 32 * h, v + 32 * h);
+                for (int h = 0; h < C::CPW / 32; ++h) tmem_ld32(lane_addr + ACC_COL + ab * TN + cg * C::CPW + 32 * h, v + 32 * h);
             } else {
                 tmem_ld32(lane_addr + ACC_COL + cg * 32, v);             // gate
                 tmem_ld32(lane_addr + ACC_COL + 128 + cg * 32, v + 32);  // up
@@ -602,13 +612,17 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             // all 32 rows of this warp inside the tile's group: TMA store; else direct
             const bool full_warp = q * 32 + 32 <= x.rows;
             const uint32_t stg = smem_u32(s.stg[(warp - EPI_WARP0) * C::NBUF]);
-            if (MODE == 0) {
-                uint32_t w[C::BOXW / 2];
+            if (C::PLAIN) {
+                uint32_t w[C::CPW / 2];
 #pragma unroll
-                for (int j = 0; j < C::BOXW / 2; ++j)
+                for (int j = 0; j < C::CPW / 2; ++j)
                     w[j] = pack_bf16x2(f2_mul(f2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), scale2));
-                emit_box<C::STAGED, C::NBUF, C::BOXW, C::TMA_STORE>(p, &tmO, stg, nbox, w, full_warp, valid, lane, row,
-                                                      x.nt * TN + cg * C::BOXW, x.row0 + q * 32);
+#pragma unroll
+                for (int hf = 0; hf < C::CPW / C::BOXW; ++hf)
+                    emit_box<C::STAGED, C::NBUF, C::BOXW, C::TMA_STORE>(p, &tmO, stg, nbox, w + hf * (C::BOXW / 2),
+                                                                         full_warp, valid, lane, row,
+                                                                         x.nt * TN + cg * C::CPW + hf * C::BOXW,
+                                                                         x.row0 + q * 32);
             } else {
                 if (valid && p.c_debug) {
                     float* cgp = p.c_debug + row * p.N + x.nt * 128 + cg * 32;
@@ -798,10 +812,12 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
     CUtensorMap ta, tb, tsfb, to;
     if (!make_codes_map(&ta, g.a_codes, g.M, g.K / 2, g.mode, BM)) return cudaErrorInvalidValue;
     const int b_rows = g.mode == 0 ? Cfg<0>::B_ROWS : Cfg<1>::B_ROWS;
+    // plain GEMMs with long K loops (4 or more stages of 256) take the 5-stage form
+    const int plain_mode = (g.K / 256 >= 4) ? 2 : 0;
     if (!make_codes_map(&tb, g.b_codes, (int64_t)g.G * g.N, g.K / 2, g.mode, b_rows)) return cudaErrorInvalidValue;
     if (!make_sfb_map(&tsfb, g.b_sf, g.goff ? g.G : 1, g.N, g.K, g.mode)) return cudaErrorInvalidValue;
     const int64_t out_cols = g.mode == 1 ? g.N / 2 : g.N;
-    const int box_cols = g.mode == 0 ? Cfg<0>::BOXW : Cfg<1>::BOXW;
+    const int box_cols = g.mode == 0 ? (plain_mode == 2 ? Cfg<2>::BOXW : Cfg<0>::BOXW) : Cfg<1>::BOXW;
     if (!make_out_map(&to, g.out, g.M, out_cols, g.ldo, box_cols)) return cudaErrorInvalidValue;
     KParams p;
     p.a_sf = g.a_sf;
@@ -825,6 +841,7 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
     // dense calls: no more pairs than units of work (m-tile pairs x n-tiles)
     const int tn = g.mode == 0 ? Cfg<0>::TN : Cfg<1>::TN;
     const int64_t dense_units = g.goff == nullptr ? ((g.M + BM - 1) / BM + 1) / 2 * (g.N / tn) : 0;
+    if (g.mode == 0 && plain_mode == 2) return launch_mode<2>(ta, tb, tsfb, to, p, num_sms, dense_units, stream);
     if (g.mode == 0) return launch_mode<0>(ta, tb, tsfb, to, p, num_sms, dense_units, stream);
     return launch_mode<1>(ta, tb, tsfb, to, p, num_sms, dense_units, stream);
 }
