@@ -168,7 +168,9 @@ __global__ void __launch_bounds__(kThreads) route_permute_kernel(RouteLaunch p) 
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int i = i0 + j * W;
-                if (i < nrows) *reinterpret_cast<uint4*>(p.a1_codes + (int64_t)(pos0 + i) * row_bytes + c) = v[j];
+                // streaming stores: the 268 MB written here would otherwise push the token rows,
+                // read 8 times each, out of L2
+                if (i < nrows) __stcs(reinterpret_cast<uint4*>(p.a1_codes + (int64_t)(pos0 + i) * row_bytes + c), v[j]);
             }
         }
     }
