@@ -533,7 +533,8 @@ def weight_quantize_leg(local):
     nbytes = n * 2 * 2 + n // 2 + n // 16  # read twice (tensor amax, then encode), codes + scales written
     del w1, w2
     torch.cuda.empty_cache()
-    return {"workload": "128 experts x (W1 1536 x 2048 + W2 2048 x 768), per-tensor scales, 2 x 128 launches pairs",
+    return {"workload": "128 experts x (W1 1536 x 2048 + W2 2048 x 768), one per-tensor scale per expert matrix "
+                        "(nvfp4_quantize_grouped: 3 launches per stack)",
             "ms": ms, "gbs": nbytes / (ms / 1e3) / 1e9}
 
 

@@ -150,6 +150,26 @@ NVFP4_API int nvfp4_quantize_rows(const void* x_bf16, int64_t rows, int64_t cols
                         void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * nvfp4_quantize_grouped: quantize `groups` bf16 matrices stacked row-wise,
+ * x [groups * rows_per_group x cols] (contiguous, row stride cols), each
+ * with its own per-tensor outer scale (scale_mode must contain
+ * NVFP4_PER_TENSOR; four-over-six flags as in nvfp4_quantize_rows): the
+ * per-expert weights of an MoE layer, requantized after every optimizer
+ * step.  Bit-identical to nvfp4_quantize_rows(NVFP4_PER_TENSOR) on each
+ * group, in three launches for all groups instead of three per group.
+ * out: rows = groups * rows_per_group, cols = cols; out->scale has `groups`
+ * entries; the swizzled block scales of group g start at byte g *
+ * nvfp4_sf_bytes(rows_per_group, cols).
+ * Shapes: 1 <= groups <= 65535, rows_per_group % 128 == 0, rows_per_group
+ *         >= 128, 0 < cols <= 32768, cols % 16 == 0.
+ * ws: >= 16 + 4 * groups bytes, 16-byte aligned (error word, then the
+ * groups' amax accumulators).
+ */
+NVFP4_API int nvfp4_quantize_grouped(const void* x_bf16, int groups, int64_t rows_per_group, int64_t cols,
+                                     int scale_mode, const nvfp4_tensor* out, void* ws, size_t ws_bytes,
+                                     void* stream);
+
+/*
  * nvfp4_dequantize_rows: y[r][j] = bf16(q[r][j] * s_b[r][j/16] * s_g) for an
  * NVFP4 matrix `in` [rows x cols] as nvfp4_quantize_rows writes it (swizzled
  * block scales), rounded once to nearest even from the exact product.  This

@@ -47,7 +47,8 @@ class _Layout(ctypes.Structure):
 PER_ROW = 0
 PER_TENSOR = 1
 FOUR_OVER_SIX = {None: 0, "mse": 2, "mae": 4}  # scale-mode flags of four-over-six block scaling
-SYMBOLS = ["nvfp4_sf_bytes", "nvfp4_quantize_workspace", "nvfp4_quantize_rows", "nvfp4_dequantize_rows",
+SYMBOLS = ["nvfp4_sf_bytes", "nvfp4_quantize_workspace", "nvfp4_quantize_rows", "nvfp4_quantize_grouped",
+           "nvfp4_dequantize_rows",
            "nvfp4_linear",
            "moe_expert_workspace_layout", "moe_expert_workspace", "moe_expert_forward",
            "moe_expert_forward_noalloc", "nvfp4_last_error"]
@@ -77,6 +78,9 @@ def lib():
         L.nvfp4_quantize_rows.restype = ctypes.c_int
         L.nvfp4_quantize_rows.argtypes = [c_vp, c_i64, c_i64, c_i64, ctypes.c_int, c_vp,
                                           ctypes.POINTER(_Tensor), c_vp, ctypes.c_size_t, c_vp]
+        L.nvfp4_quantize_grouped.restype = ctypes.c_int
+        L.nvfp4_quantize_grouped.argtypes = [c_vp, ctypes.c_int, c_i64, c_i64, ctypes.c_int, ctypes.POINTER(_Tensor),
+                                             c_vp, ctypes.c_size_t, c_vp]
         L.nvfp4_dequantize_rows.restype = ctypes.c_int
         L.nvfp4_dequantize_rows.argtypes = [ctypes.POINTER(_Tensor), ctypes.c_int, c_vp, c_vp, ctypes.c_int, c_vp,
                                             c_i64, c_vp]
@@ -177,17 +181,12 @@ def quantize_grouped_weights(w, four_over_six=None, stream=None):
     with one per-tensor scale per expert (scale has G entries).  Requires
     N % 128 == 0 so each expert's swizzled scales are a contiguous slice."""
     G, N, K = w.shape
-    assert N % 128 == 0
+    assert N % 128 == 0 and w.is_contiguous()
     out = NVFP4Tensor.empty(G * N, K, G, w.device)
-    per_sf = sf_bytes(N, K)
-    ws = torch.empty(256, dtype=torch.uint8, device=w.device)
-    for g in range(G):
-        sub = _Tensor(out.codes.data_ptr() + g * N * (K // 2), out.sf.data_ptr() + g * per_sf,
-                      out.scale.data_ptr() + 4 * g, N, K)
-        rc = lib().nvfp4_quantize_rows(_ptr(w[g]), N, K, K, PER_TENSOR | FOUR_OVER_SIX[four_over_six], None,
-                                       ctypes.byref(sub),
-                                       _ptr(ws), 256, _stream(stream))
-        _check(rc, "nvfp4_quantize_rows (weights)")
+    ws = torch.empty(16 + 4 * G, dtype=torch.uint8, device=w.device)
+    rc = lib().nvfp4_quantize_grouped(_ptr(w), G, N, K, PER_TENSOR | FOUR_OVER_SIX[four_over_six], ctypes.byref(out.c()),
+                                      _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "nvfp4_quantize_grouped")
     return out
 
 

@@ -122,6 +122,42 @@ int nvfp4_quantize_rows(const void* x_bf16, int64_t rows, int64_t cols, int64_t 
     return ok();
 }
 
+int nvfp4_quantize_grouped(const void* x_bf16, int groups, int64_t rows_per_group, int64_t cols, int scale_mode,
+                           const nvfp4_tensor* out, void* ws, size_t ws_bytes, void* stream) {
+    if (x_bf16 == nullptr) return fail(NVFP4_EINVAL, "quantize grouped: x is null");
+    if (!(scale_mode & NVFP4_PER_TENSOR) || !fos_flags_valid(scale_mode & ~NVFP4_PER_TENSOR))
+        return fail(NVFP4_EINVAL, "quantize grouped: scale_mode must be NVFP4_PER_TENSOR (| four-over-six)");
+    int rc = check_tensor(out, "quantize grouped out");
+    if (rc) return rc;
+    if (groups < 1 || groups > 65535) return fail(NVFP4_ESHAPE, "quantize grouped: groups must be in [1, 65535]");
+    if (rows_per_group < 128 || rows_per_group % 128 != 0)
+        return fail(NVFP4_ESHAPE, "quantize grouped: rows_per_group must be a positive multiple of 128");
+    if (cols <= 0 || cols % 16 != 0 || cols > 32768)
+        return fail(NVFP4_ESHAPE, "quantize grouped: cols must be a multiple of 16 in (0, 32768]");
+    const int64_t rows = (int64_t)groups * rows_per_group;
+    if (rows >= (1ll << 31)) return fail(NVFP4_ESHAPE, "quantize grouped: too many rows");
+    if (out->rows != rows || out->cols != cols) return fail(NVFP4_EINVAL, "quantize grouped: out shape mismatch");
+    if (!aligned(x_bf16, 16)) return fail(NVFP4_EALIGN, "quantize grouped: x must be 16-byte aligned");
+    if (ws == nullptr || !aligned(ws, 16) || ws_bytes < 16 + 4 * (size_t)groups)
+        return fail(NVFP4_EWORKSPACE, "quantize grouped: ws must hold 16 + 4 * groups bytes, 16-byte aligned");
+    nvfp4::QuantLaunch q{};
+    q.x = x_bf16;
+    q.ld = cols;
+    q.rows = rows;
+    q.cols = cols;
+    q.per_tensor = 1;
+    q.groups = groups;
+    q.fos = fos_of(scale_mode);
+    q.codes = out->codes;
+    q.sf = out->sf;
+    q.scale = out->scale;
+    q.ws = ws;
+    q.err = reinterpret_cast<uint32_t*>(ws);
+    cudaError_t e = nvfp4::launch_quantize(q, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(NVFP4_ELAUNCH, "quantize grouped: %s", cudaGetErrorString(e));
+    return ok();
+}
+
 int nvfp4_dequantize_rows(const nvfp4_tensor* in, int scale_mode, const int* group_offsets,
                           const int* padded_offsets, int groups, void* y_bf16, int64_t ldy, void* stream) {
     if (in != nullptr && in->rows == 0 && in->cols > 0 && in->cols % 16 == 0) return ok();  // nothing to write

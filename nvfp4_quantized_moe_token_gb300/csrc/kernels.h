@@ -21,7 +21,8 @@ struct QuantLaunch {
     int G;
     int reverse;            // rows taken last to first
     int fos;                // four-over-six: 0 off, 1 by MSE, 2 by MAE
-    void* ws;               // >= 4 bytes when per_tensor && !amax_in
+    int groups;             // per_tensor: one outer scale per group of rows / groups rows (0 or 1: one)
+    void* ws;               // >= 16 + 4 * groups bytes when per_tensor && !amax_in
     uint32_t* err;          // nullable device error word (pipeline wait time-outs)
 };
 cudaError_t launch_quantize(const QuantLaunch& q, cudaStream_t stream);

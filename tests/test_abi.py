@@ -105,3 +105,18 @@ def test_moe_rejects_bad_arguments(L):
     assert call(ws=4096 + 16) == -3
     assert call(x=None) == -1
     assert call(T=0) == -1
+
+
+def test_quantize_grouped_rejects_bad_arguments(L):
+    """Host-side checks of nvfp4_quantize_grouped (no device work happens)."""
+    def call(groups=4, rpg=256, cols=64, mode=1, ws=4096, wsb=64, rows=None):
+        out = _t(groups * rpg if rows is None else rows, cols)
+        return L.nvfp4_quantize_grouped(4096, groups, rpg, cols, mode, ctypes.byref(out), ws, wsb, None)
+    assert call(mode=0) == -1            # per-tensor scales only
+    assert call(groups=0) == -2
+    assert call(rpg=200) == -2           # rows per group: multiples of 128
+    assert call(cols=40) == -2
+    assert call(rows=100) == -1          # out shape
+    assert call(wsb=16 + 4 * 4 - 1) == -4
+    assert call(ws=None) == -4
+    assert L.nvfp4_last_error().decode()

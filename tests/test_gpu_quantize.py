@@ -133,3 +133,22 @@ def test_quant_strided_and_offset_rows():
     got = nv.quantize_rows(dev)
     torch.cuda.synchronize()
     assert_quant_equal(got, oracle.quantize(x), rows, cols, what="base 16 bytes off a 32-byte boundary")
+
+
+@pytest.mark.parametrize("fos", [None, "mse"])
+def test_quant_grouped_per_tensor_matches_each_group(fos):
+    """nvfp4_quantize_grouped: G expert matrices, each with its own per-tensor
+    scale (different magnitudes, one all-zero group), bit-identical to the
+    oracle's per-tensor quantization of every group."""
+    G, N, K = 5, 256, 768
+    rng = np.random.default_rng(17)
+    ws = [workloads.gaussian_bf16(rng, (N, K), std=s) for s in (0.02, 1.0, 0.0, 3e-5, 40.0)]
+    w = np.stack(ws)
+    wt = to_dev_bf16(w.reshape(G * N, K)).view(G, N, K)
+    got = nv.quantize_grouped_weights(wt, four_over_six=fos)
+    torch.cuda.synchronize()
+    per = nv.sf_bytes(N, K)
+    for g in range(G):
+        ref = oracle.quantize(w[g], per_tensor=True) if fos is None else oracle.quantize_46(w[g], err=fos, per_tensor=True)
+        sub = nv.NVFP4Tensor(got.codes[g * N:(g + 1) * N], got.sf[g * per:(g + 1) * per], got.scale[g:g + 1], N, K)
+        assert_quant_equal(sub, ref, N, K, what=f"group {g} ({fos})")
