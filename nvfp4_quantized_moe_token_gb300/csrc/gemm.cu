@@ -138,8 +138,7 @@ struct __align__(1024) Smem {
     uint64_t sf_full[C::STAGES];   // (even CTA) scales of the stage in TMEM: 4 warps of each CTA
     uint64_t empty[C::STAGES];     // MMAs of the stage done (commit, multicast to the pair)
     uint64_t tmem_full[C::ACC_BUFS];   // accumulator ready (commit, multicast to the pair)
-    uint64_t tmem_empty[C::ACC_BUFS];  // (even CTA) accumulator drained: one arrival per CTA
-    uint64_t epi_done[C::ACC_BUFS];    // this CTA's 16 epilogue warps copied that accumulator out
+    uint64_t tmem_empty[C::ACC_BUFS];  // (even CTA) accumulator drained: one arrival per epilogue warp of the pair
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -374,9 +373,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         }
         for (int i = 0; i < ACC_BUFS; ++i) {
             mbar_init(smem_u32(&s.tmem_full[i]), 1);
-            mbar_init(smem_u32(&s.tmem_empty[i]), 2);
-            // per accumulator: a warp's arrival for tile t + ACC_BUFS waits for tile t's release
-            mbar_init(smem_u32(&s.epi_done[i]), EPI_WARPS);
+            mbar_init(smem_u32(&s.tmem_empty[i]), 2 * EPI_WARPS);
         }
         mbar_init(smem_u32(&s.drain), 1);
         s.abort = 0;
@@ -559,10 +556,11 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         if (!ok && lane == 0) raise_abort(&s.abort, rank);
     } else if (warp < PRODB_WARP) {
         // ---------------------------------------------------------------- epilogue
-        // Each warp copies its 32 rows x (64 in mode 1, 32 in mode 0)
-        // accumulator columns into registers; once all 16 have, warp 6
-        // releases the CTA's half of that accumulator with one arrival, so the
-        // MMAs that need it can run while the warps scale, activate and store.
+        // Each warp copies its 32 rows x 64 accumulator columns into
+        // registers (mode 1: 32 gate and the matching 32 up columns) and
+        // releases them with one arrival on the even CTA's tmem_empty, so the
+        // MMAs that need the accumulator can run while the warps scale,
+        // activate and store.
         const int q = warp & 3;                    // TMEM lane quarter this warp may access
         const int cg = (warp - EPI_WARP0) >> 2;    // column group 0..3
         const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
@@ -593,19 +591,11 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&s.epi_done[ab]));
-            if (warp == EPI_WARP0) {
-                if (lane == 0) {
-                    if (mbar_wait_bounded(smem_u32(&s.epi_done[ab]), acc_phase, abort, p.err)) {
-                        tc_fence_after();
-                        mbar_arrive_cluster(mapa_shared(smem_u32(&s.tmem_empty[ab]), 0));
-                    } else {
-                        ok = false;
-                    }
-                }
-                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-                if (!ok) break;
-            }
+            // Each warp releases its share of the accumulator itself: an arrival
+            // on the even CTA's barrier, which completes when all 32 warps of
+            // the pair have theirs in registers.  A warp arrives for tile t + 1
+            // only after tile t + 1's commit, which follows that completion.
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&s.tmem_empty[ab]), 0));
             if (x.rows == 0) continue;  // the odd CTA of a group's last pair: nothing to store
             const float scale = __fmul_rn(sa, sbw);
             const uint64_t scale2 = f2(scale, scale);
