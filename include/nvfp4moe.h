@@ -315,7 +315,7 @@ NVFP4_API int moe_expert_forward(const void* x_bf16, int64_t T, int64_t H,
  *   until the process exits.  Sizes whose workspace
  *   (moe_expert_workspace()) exceeds 32 MiB are rejected with
  *   NVFP4_EWORKSPACE and a message; at hidden 2048, FFN 768, 128 experts,
- *   top-8 that is more than 512 tokens.
+ *   top-8 that is more than 518 tokens.
  *   The first call on each device looks the array's device address up
  *   (cudaGetSymbolAddress) with that device current, so make it before any
  *   stream capture.  Nothing is allocated, by this call or later ones.
