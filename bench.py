@@ -361,14 +361,43 @@ def run_ours(args, rank, world, local):
     return res, d
 
 
+def _graph_per_launch(calls, replays, dev):
+    """Device time per kernel of `calls` (callables that each enqueue one
+    launch on the current stream), captured once into a CUDA graph and
+    replayed back to back: the kernels' own rate, without the host-side
+    cost of each Python call between them."""
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        for c in calls:
+            c()
+    torch.cuda.current_stream(dev).wait_stream(side)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(replays):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / (replays * len(calls))
+    del g
+    return ms
+
+
 def quant_gbs(args, local, reps=50, four_over_six=None):
-    """Quantizer throughput on the 16384 x 2048 per-token workload.  Two
-    measurements: launches back to back over 4 rotating copies of the input
-    and outputs (256 MiB of input > L2, so every launch reads its rows from
-    DRAM), timed per group of 4 launches (the headline: the kernel's own
-    rate); and single launches with the L2 flushed before each (adds the
-    launch and event overhead of one small kernel).  four_over_six 'mse' /
-    'mae' times the four-over-six quantizer on the same rows."""
+    """Quantizer throughput on the 16384 x 2048 per-token workload, over 4
+    rotating copies of the input and outputs (256 MiB of input > L2, so
+    every launch reads its rows from DRAM).  Three measurements: the
+    launches captured in a CUDA graph and replayed back to back (the
+    headline: the kernel's own rate); the same launches issued one Python
+    call at a time (adds the host-side cost of each call wherever it exceeds
+    the kernel's ~17 us); and single launches with the L2 flushed before
+    each (adds the launch and event overhead of one small kernel).
+    four_over_six 'mse' / 'mae' times the four-over-six quantizer on the
+    same rows."""
     import nvfp4_quantized_moe_token_gb300 as nv
     dev = torch.device("cuda", local)
     xb = workloads.quant_rows()["x"]
@@ -391,7 +420,9 @@ def quant_gbs(args, local, reps=50, four_over_six=None):
         groups.append((a, b))
     torch.cuda.synchronize()
     torch.cuda.nvtx.range_pop()
-    ms = statistics.fmean(a.elapsed_time(b) for a, b in groups) / 4
+    ms_calls = statistics.fmean(a.elapsed_time(b) for a, b in groups) / 4
+    calls = [lambda i=i: nv.quantize_rows(xs[i], out=qs[i], four_over_six=four_over_six) for i in range(4)] * 4
+    ms = _graph_per_launch(calls, max(reps // 16, 4), dev)
     ts = []
     for _ in range(reps):
         flush()
@@ -412,7 +443,9 @@ def quant_gbs(args, local, reps=50, four_over_six=None):
     gbs = nbytes / (ms / 1e3) / 1e9
     out = {"workload": "quantize 16384 x 2048" + ("" if four_over_six is None else f", four-over-six ({four_over_six})"),
            "us": ms * 1e3, "gbs": gbs, "algorithmic_bytes": nbytes, "frac_of_hbm": gbs / hbm, "hbm_peak_gbs": hbm,
-           "timing": "back-to-back launches over 4 rotating input/output copies (256 MiB of input > L2), per launch",
+           "timing": "launches over 4 rotating input/output copies (256 MiB of input > L2) captured in a CUDA "
+                     "graph and replayed back to back, per launch",
+           "us_python_calls": ms_calls * 1e3, "frac_of_hbm_python_calls": nbytes / (ms_calls / 1e3) / 1e9 / hbm,
            "us_single_launch_l2_flushed": ms_single * 1e3,
            "frac_of_hbm_single_launch": nbytes / (ms_single / 1e3) / 1e9 / hbm}
     if four_over_six is None:
@@ -424,10 +457,11 @@ def quant_gbs(args, local, reps=50, four_over_six=None):
 
 def dequant_gbs(args, local, reps=50):
     """DQ(Q(x)) throughput: the 16384 x 2048 workload quantized once, then
-    dequantized to bf16 back to back over 8 rotating input/output copies
-    (656 MB per rotation > L2, so every launch reads its codes from DRAM),
-    timed per group of 8 launches; plus single launches with the L2 flushed
-    before each."""
+    dequantized to bf16 over 8 rotating input/output copies (656 MB per
+    rotation > L2, so every launch reads its codes from DRAM): launches
+    captured in a CUDA graph and replayed back to back (the headline), the
+    same launches one Python call at a time, and single launches with the L2
+    flushed before each."""
     import nvfp4_quantized_moe_token_gb300 as nv
     dev = torch.device("cuda", local)
     xb = workloads.quant_rows()["x"]
@@ -450,7 +484,9 @@ def dequant_gbs(args, local, reps=50):
         groups.append((a, b))
     torch.cuda.synchronize()
     torch.cuda.nvtx.range_pop()
-    ms = statistics.fmean(a.elapsed_time(b) for a, b in groups) / 8
+    ms_calls = statistics.fmean(a.elapsed_time(b) for a, b in groups) / 8
+    calls = [lambda i=i: nv.dequantize_rows(qs[i], out=ys[i]) for i in range(8)] * 2
+    ms = _graph_per_launch(calls, max(reps // 16, 4), dev)
     single = _timed(lambda: nv.dequantize_rows(qs[0], out=ys[0]), reps, flush)
     nbytes = 16384 * (1024 + 128 + 4 + 2048 * 2)  # codes, scales, row scale in; bf16 out
     hbm = 6800.0
@@ -463,8 +499,8 @@ def dequant_gbs(args, local, reps=50):
     torch.cuda.empty_cache()
     return {"workload": "dequantize (DQ(Q(x)) -> bf16) 16384 x 2048", "us": ms * 1e3, "gbs": gbs,
             "algorithmic_bytes": nbytes, "frac_of_hbm": gbs / hbm, "hbm_peak_gbs": hbm,
-            "timing": "back-to-back launches over 8 rotating copies, per launch",
-            "us_single_launch_l2_flushed": single * 1e3}
+            "timing": "launches over 8 rotating copies captured in a CUDA graph and replayed back to back, per launch",
+            "us_python_calls": ms_calls * 1e3, "us_single_launch_l2_flushed": single * 1e3}
 
 
 def _timed(fn, reps, flush=None):
