@@ -230,6 +230,13 @@ typedef struct moe_debug {
      * (with the router top-k, launched together), routing metadata +
      * permute, FC1, requant, FC2, combine. */
     void** stage_events;
+    /* Nonzero: FC1's MMA-issuing thread first waits on a barrier that
+     * nothing arrives at, so that its bounded wait runs out (a test of the
+     * time-out path).  The kernel then sets NVFP4_DEVERR_TIMEOUT in the
+     * workspace's error word, stops all its roles, frees its tensor memory
+     * and returns; the layer's outputs are undefined, the context stays
+     * usable.  Takes about 2 s.  0 for normal operation. */
+    int stall_fc1;
 } moe_debug;
 
 #define MOE_STAGE_EVENTS 7

@@ -29,7 +29,7 @@ class _Options(ctypes.Structure):
 
 
 class _Debug(ctypes.Structure):
-    _fields_ = [("fc1_out", c_vp), ("stage_events", ctypes.POINTER(c_vp))]
+    _fields_ = [("fc1_out", c_vp), ("stage_events", ctypes.POINTER(c_vp)), ("stall_fc1", ctypes.c_int)]
 
 
 STAGES = ["quantize", "route", "fc1", "requant", "fc2", "combine"]
@@ -46,6 +46,8 @@ class _Layout(ctypes.Structure):
 
 PER_ROW = 0
 PER_TENSOR = 1
+DEVERR_TIMEOUT = 1    # bits of the device error word
+DEVERR_BADEXPERT = 2
 FOUR_OVER_SIX = {None: 0, "mse": 2, "mae": 4}  # scale-mode flags of four-over-six block scaling
 SYMBOLS = ["nvfp4_sf_bytes", "nvfp4_quantize_workspace", "nvfp4_quantize_rows", "nvfp4_quantize_grouped",
            "nvfp4_dequantize_rows",
@@ -210,9 +212,13 @@ def moe_workspace_layout(T, H, F, E, topk):
 
 
 def moe_expert_forward(x, logits, bias, w1q, w2q, F, topk, weight_at_fc1=False, out=None,
-                       ws=None, fc1_debug=None, stage_events=None, four_over_six=None, stream=None):
+                       ws=None, fc1_debug=None, stage_events=None, four_over_six=None, stream=None,
+                       debug_stall_fc1=False):
     """One W4A4 MoE expert layer on the device.  Returns (out bf16 [T, H], ws).
     four_over_six (None, 'mse', 'mae'): four-over-six scaling of the activations.
+    debug_stall_fc1: test of the time-out path (moe_debug.stall_fc1): FC1's
+    bounded wait runs out, DEVERR_TIMEOUT is set in the workspace's error
+    word, the outputs are undefined.
 
     stage_events (optional): len(STAGES) + 1 torch.cuda.Event objects (or None
     for an event to skip) recorded on the stream before the first stage and
@@ -234,7 +240,7 @@ def moe_expert_forward(x, logits, bias, w1q, w2q, F, topk, weight_at_fc1=False, 
             if e is not None and e.cuda_event == 0:  # torch creates the CUDA event on its first record
                 e.record(st)
         evs = (c_vp * len(stage_events))(*[None if e is None else e.cuda_event for e in stage_events])
-    dbg = _Debug(None if fc1_debug is None else fc1_debug.data_ptr(), evs)
+    dbg = _Debug(None if fc1_debug is None else fc1_debug.data_ptr(), evs, 1 if debug_stall_fc1 else 0)
     rc = lib().moe_expert_forward(_ptr(x), T, H, _ptr(logits), _ptr(bias), E, topk, ctypes.byref(a),
                                   ctypes.byref(b), F, ctypes.byref(opt), _ptr(out), ctypes.byref(dbg),
                                   _ptr(ws), ws.numel(), _stream(stream))

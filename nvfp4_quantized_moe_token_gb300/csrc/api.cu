@@ -401,6 +401,7 @@ int moe_expert_forward(const void* x_bf16, int64_t T, int64_t H, const float* ro
     g1.amax_out = reinterpret_cast<float*>(at(L.amax2));
     g1.row_prob = r.row_w;
     g1.c_debug = dbg ? dbg->fc1_out : nullptr;
+    g1.stall = dbg ? dbg->stall_fc1 : 0;
     g1.err = r.err;
     g1.num_sms = sm_count();
     if ((e = nvfp4::launch_gemm(g1, s)) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe fc1: %s", cudaGetErrorString(e));

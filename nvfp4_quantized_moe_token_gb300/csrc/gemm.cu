@@ -140,6 +140,7 @@ struct __align__(1024) Smem {
     uint64_t tmem_full[C::ACC_BUFS];   // accumulator ready (commit, multicast to the pair)
     uint64_t tmem_empty[C::ACC_BUFS];  // (even CTA) accumulator drained: one arrival per epilogue warp of the pair
     uint64_t drain;
+    uint64_t never;                // no arrival ever: the time-out test's wait
     uint32_t tmem_base;
     int abort;
     int goff[MAX_G + 1];
@@ -171,6 +172,7 @@ struct KParams {
     const float* row_prob;
     float* c_debug;
     uint32_t* err;
+    int stall;
 };
 
 struct Tile {
@@ -376,6 +378,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             mbar_init(smem_u32(&s.tmem_empty[i]), 2 * EPI_WARPS);
         }
         mbar_init(smem_u32(&s.drain), 1);
+        mbar_init(smem_u32(&s.never), 1);
         s.abort = 0;
         fence_barrier_init();
     }
@@ -480,6 +483,8 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             int stage = 0, it = 0;
             uint32_t phase = 0;
             bool ok = true;
+            // the time-out test: a bounded wait for a phase that never completes
+            if (p.stall) ok = mbar_wait_bounded_relaxed(smem_u32(&s.never), 0, abort, p.err);
             for (int u = pair; u < total && ok; u += n_pairs, ++it) {
                 // accumulator it % ACC_BUFS, in its (it / ACC_BUFS)-th use
                 const int ab = ACC_BUFS == 1 ? 0 : (it & 1);
@@ -827,6 +832,7 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
     p.row_prob = g.row_prob;
     p.c_debug = g.c_debug;
     p.err = g.err;
+    p.stall = g.stall;
     const int num_sms = g.num_sms > 0 ? g.num_sms : 148;
     // dense calls: no more pairs than units of work (m-tile pairs x n-tiles)
     const int tn = g.mode == 0 ? Cfg<0>::TN : Cfg<1>::TN;

@@ -67,6 +67,7 @@ struct GemmLaunch {
     float* c_debug;        // mode 1, nullable: fp32 [M x N] pre-activation
     uint32_t* err;         // nullable
     int num_sms;
+    int stall;             // test of the time-out path: the MMA thread waits on a barrier nothing arrives at
 };
 cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t stream);
 

@@ -30,6 +30,24 @@ def test_header_declares_the_binding_symbols():
     assert sorted(declared_functions()) == sorted(nv.SYMBOLS)
 
 
+def _struct_fields(src, name):
+    """Field names, in order, of `typedef struct name { ... } name;` in the header."""
+    body = re.search(r"typedef struct " + name + r" \{(.*?)\} " + name + ";", src, re.S).group(1)
+    return re.findall(r"(\w+)\s*;", re.sub(r"/\*.*?\*/", "", body, flags=re.S))
+
+
+def test_binding_structs_and_error_bits_match_the_header():
+    """The ctypes structures mirror the header field by field (a mismatch would
+    shift every later field silently), and the error-word bits agree."""
+    src = open(HEADER).read()
+    assert _struct_fields(src, "moe_debug") == [f[0] for f in nv._Debug._fields_]
+    assert _struct_fields(src, "moe_workspace_layout") == nv.LAYOUT_FIELDS
+    assert _struct_fields(src, "moe_options") == [f[0] for f in nv._Options._fields_]
+    assert _struct_fields(src, "nvfp4_tensor") == [f[0] for f in nv._Tensor._fields_]
+    bits = dict(re.findall(r"#define NVFP4_DEVERR_(\w+) (\d+)u", src))
+    assert int(bits["TIMEOUT"]) == nv.DEVERR_TIMEOUT and int(bits["BADEXPERT"]) == nv.DEVERR_BADEXPERT
+
+
 def test_every_declared_symbol_is_exported(L):
     for name in declared_functions():
         assert hasattr(L, name), name
