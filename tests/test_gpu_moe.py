@@ -179,7 +179,14 @@ def small_layer(T, E, k, H, F, seed, bias_std=1.0):
 
 
 @pytest.mark.parametrize("T,E,k,H,F", [(1000, 32, 4, 512, 256), (1, 32, 2, 256, 128), (129, 64, 8, 256, 384),
-                                         (129, 128, 8, 1024, 128), (33, 128, 8, 2048, 256)])
+                                         (129, 128, 8, 1024, 128), (33, 128, 8, 2048, 256),
+                                         # top-1 (router weight exactly 1), E = 96 (3 logits per lane)
+                                         (200, 96, 1, 512, 256),
+                                         # the largest E and top-k the library accepts (256, 16): most
+                                         # experts get 0-10 rows; the combine's 16-slot instance
+                                         (64, 256, 16, 256, 128),
+                                         # E = 160 (5 logits per lane), top-16
+                                         (40, 160, 16, 256, 128)])
 def test_moe_small_full_and_end_to_end(T, E, k, H, F):
     d = small_layer(T, E, k, H, F, seed=T + E)
     dev = run_device(d, E, k, F)
