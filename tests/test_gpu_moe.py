@@ -201,6 +201,44 @@ def test_moe_small_full_and_end_to_end(T, E, k, H, F):
     assert rel <= 2e-3, rel
 
 
+def test_moe_zero_and_outlier_tokens_and_a_zero_expert():
+    """Degenerate rows through the whole layer: all-zero tokens (s_g = 0, zero
+    codes and block scales), x50 outlier entries (block scales near E4M3
+    saturation), and an expert whose W1 is all zero, so that its rows reach
+    the requant with amax 0 (zero codes, scales and outer scale) and FC2 with
+    zero operands; those tokens' outputs then sum only their other slots."""
+    T, E, k, H, F = 400, 64, 4, 512, 256
+    rng = np.random.default_rng(41)
+    d = dict(x=workloads.gaussian_bf16(rng, (T, H), outlier_frac=0.02, outlier_mult=50.0, zero_row_frac=0.05),
+             logits=rng.standard_normal((T, E), dtype=np.float32),
+             bias=rng.standard_normal(E, dtype=np.float32),
+             w1=workloads.gaussian_bf16(rng, (E, 2 * F, H), std=0.02),
+             w2=workloads.gaussian_bf16(rng, (E, H, F), std=0.02))
+    zero_e = 3
+    d["w1"][zero_e] = 0       # bf16 +0.0 everywhere
+    d["bias"][zero_e] = 3.0   # route plenty of rows to it
+    zero_tok = np.nonzero(~d["x"].any(axis=1))[0]
+    assert len(zero_tok) > 0
+    dev = run_device(d, E, k, F)
+    check_stagewise(d, E, k, F, dev)
+    m = oracle.route_metadata(oracle.route(d["logits"], d["bias"], k)[0], E)
+    lo, hi = int(m["off"][zero_e]), int(m["off"][zero_e + 1])
+    assert hi - lo > 0
+    ws, lay = dev["ws"], dev["lay"]
+    R = T * k
+    assert not ws_np(ws, lay, "amax2", np.float32, R)[lo:hi].any()
+    assert not ws_np(ws, lay, "a2_scale", np.float32, R)[lo:hi].any()
+    assert not ws_rows(ws, lay, "a2_codes", np.uint8, R, F // 2, np.arange(lo, hi)).any()
+    # all-zero tokens: every one of their slots is zero through the layer, output exactly zero
+    assert np.all((dev["out"][zero_tok] & 0x7FFF) == 0)
+    w1o = [oracle.quantize(d["w1"][e], per_tensor=True) for e in range(E)]
+    w2o = [oracle.quantize(d["w2"][e], per_tensor=True) for e in range(E)]
+    ref = oracle.moe_forward(d["x"], d["logits"], d["bias"], w1o, w2o, k)
+    g = oracle.bf16_to_f64(dev["out"])
+    r = oracle.bf16_to_f64(ref["out"])
+    assert np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-30) <= 2e-3
+
+
 def test_moe_weight_at_fc1_variant():
     T, E, k, H, F = 300, 32, 4, 512, 256
     d = small_layer(T, E, k, H, F, seed=11)
