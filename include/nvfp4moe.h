@@ -219,7 +219,9 @@ typedef struct moe_options {
     int four_over_six;
 } moe_options;
 
-/* Optional debug outputs of moe_expert_forward (all nullable, device). */
+/* Optional debug outputs of moe_expert_forward (all nullable, device).
+ * Zero-initialise the whole struct (moe_debug d = {0};) and set only the
+ * fields wanted: every field's zero value means "off". */
 typedef struct moe_debug {
     /* fp32 [R x 2F], R = T*topk rows in expert order: the FC1 output after
      * the alpha scaling, before SwiGLU (gate columns then up columns). */
