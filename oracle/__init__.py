@@ -110,9 +110,12 @@ def bf16_to_f64(h):
 
 
 def bf16_ulp(y):
-    """Spacing of bf16 numbers at |y|: 2^(floor(log2|y|) - 7), 2^-133 below 2^-126."""
+    """Spacing of bf16 numbers at |y|: the gap from the bf16 binade holding |y|
+    to its next value, 2^(floor(log2|y|) - 7), and the subnormal spacing 2^-133
+    below 2^-126 (zero included).  floor(log2|y|) is read exactly off frexp."""
     a = np.abs(np.asarray(y, np.float64))
-    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    _, ex = np.frexp(a)  # a = m 2^ex, 0.5 <= m < 1, so floor(log2 a) = ex - 1 (a > 0)
+    e = np.where(a > 0, ex.astype(np.float64) - 1.0, -126.0)
     e = np.maximum(e, -126.0)
     return np.exp2(e - 7.0)
 

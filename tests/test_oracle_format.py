@@ -270,3 +270,24 @@ def test_dequantize_hand_values():
     codes16[0, :2] = codes[0]
     out = oracle.dequantize(codes16, sf, scale)
     assert out[0, :4].tolist() == [0.5, 3.0, 0.25, -3.0]
+
+
+def test_bf16_ulp_is_the_gap_to_the_next_bf16_value():
+    """oracle.bf16_ulp, the unit of every bf16 tolerance, against the spacing
+    read off consecutive bf16 bit patterns: for every non-negative finite
+    pattern, the distance to the next pattern's value (the largest finite
+    value takes the gap below it), at the value itself, at points strictly
+    inside the gap, and for the negated value."""
+    b = np.arange(0, 0x7F80, dtype=np.uint32)  # +0 .. largest finite, as bit patterns
+    v = (b << 16).view(np.float32).astype(np.float64)
+    nxt = ((b + 1) << 16).view(np.float32).astype(np.float64)  # 0x7F80 is +inf
+    gap = nxt - v
+    gap[-1] = v[-1] - v[-2]
+    assert np.array_equal(oracle.bf16_ulp(v), gap)
+    assert np.array_equal(oracle.bf16_ulp(-v), gap)
+    inside = v[:-1] + gap[:-1] * 0.75  # strictly between two neighbours (exact in fp64)
+    assert np.all((inside > v[:-1]) & (inside < nxt[:-1]))
+    assert np.array_equal(oracle.bf16_ulp(inside), gap[:-1])
+    # the smallest subnormal spacing holds from zero through the top of the subnormal range
+    assert oracle.bf16_ulp(0.0) == 2.0 ** -133 and oracle.bf16_ulp(2.0 ** -126) == 2.0 ** -133
+    assert oracle.bf16_ulp(1.0) == 2.0 ** -7 and oracle.bf16_ulp(np.nextafter(2.0, 0.0)) == 2.0 ** -7
