@@ -314,7 +314,7 @@ def combine(y, inv, w):
     return out
 
 
-def moe_forward(x_bf16, logits, bias, w1q, w2q, k, rows=None, w_deq=None):
+def moe_forward(x_bf16, logits, bias, w1q, w2q, k, rows=None, w_deq=None, with_abs=False):
     """Whole expert layer on the CPU, each stage from the previous oracle stage.
 
     w1q / w2q: lists over experts of (codes, sf_lin, scale[1]) per-tensor
@@ -323,7 +323,11 @@ def moe_forward(x_bf16, logits, bias, w1q, w2q, k, rows=None, w_deq=None):
     metadata and every expert GEMM row needed by them are still computed).
     w_deq (nullable): (list of dequantize(w1q[e]), list of dequantize(w2q[e]))
     computed once for static weights.
-    Returns a dict of every intermediate."""
+    with_abs: also return sum_k |a_k b_k| of FC2 for every computed element
+    (the term of the GEMM tolerance).
+    Returns a dict of every intermediate; the per-row ones (D, amax2,
+    q2_codes, y2, y2_abs) hold the computed expert-ordered rows `rows_computed`
+    (all R rows when rows is None), in that order."""
     E = len(w1q)
     ids, w = route(logits, bias, k)
     meta = route_metadata(ids, E)
@@ -333,33 +337,95 @@ def moe_forward(x_bf16, logits, bias, w1q, w2q, k, rows=None, w_deq=None):
     R = int(off[-1])
     F = w2q[0][0].shape[1] * 2
     H = w1q[0][0].shape[1] * 2
-    need = np.ones(R, bool)
-    if rows is not None:
-        need[:] = False
-        need[meta["inv"].reshape(-1, k)[np.asarray(rows)].reshape(-1)] = True
-    y2 = np.zeros((R, H), np.float64)
-    d_all = np.zeros((R, F), np.uint16)
-    amax2 = np.zeros(R, np.float32)
+    inv_tk = meta["inv"].reshape(-1, k)
+    if rows is None:
+        need = np.arange(R, dtype=np.int64)
+    else:
+        need = np.unique(inv_tk[np.asarray(rows)].reshape(-1)).astype(np.int64)
+    at = np.full(R, -1, np.int64)  # position of an expert-ordered row among the computed ones
+    at[need] = np.arange(len(need))
+    n = len(need)
+    y2 = np.zeros((n, H), np.float64)
+    y2_abs = np.zeros((n, H), np.float64) if with_abs else None
+    d_all = np.zeros((n, F), np.uint16)
+    amax2 = np.zeros(n, np.float32)
+    q2_codes = np.zeros((n, F // 2), np.uint8)
     for e in range(E):
         lo, hi = int(off[e]), int(off[e + 1])
-        sel = np.nonzero(need[lo:hi])[0] + lo
+        sel = need[(need >= lo) & (need < hi)]
         if len(sel) == 0:
             continue
+        idx = at[sel]
         b1 = w_deq[0][e] if w_deq is not None else dequantize(*w1q[e], per_tensor=True)
         b2 = w_deq[1][e] if w_deq is not None else dequantize(*w2q[e], per_tensor=True)
         a = dequantize(a1[0][sel], a1[1][sel], a1[2][sel])
         c = gemm_f64(a, b1)
         d, am = swiglu(c)
-        d_all[sel] = d
-        amax2[sel] = am
+        d_all[idx] = d
+        amax2[idx] = am
         q2 = quantize(d, amax_in=am)
-        y2[sel] = bf16_to_f64(bf16_round(gemm_f64(dequantize(*q2), b2)))
+        q2_codes[idx] = q2[0]
+        a2 = dequantize(*q2)
+        y2[idx] = bf16_to_f64(bf16_round(gemm_f64(a2, b2)))
+        if with_abs:
+            y2_abs[idx] = abs_product_sum(a2, b2)
     if rows is None:
         out = combine(y2, meta["inv"], w)
     else:
         rows = np.asarray(rows)
-        out = combine(y2, meta["inv"].reshape(-1, k)[rows].reshape(-1), w[rows])
-    return dict(ids=ids, w=w, meta=meta, xq=xq, a1=a1, D=d_all, amax2=amax2, y2=y2, out=out)
+        out = combine(y2, at[inv_tk[rows].reshape(-1)].astype(np.int32), w[rows])
+    return dict(ids=ids, w=w, meta=meta, xq=xq, a1=a1, rows_computed=need, D=d_all, amax2=amax2,
+                q2_codes=q2_codes, y2=y2, y2_abs=y2_abs, out=out)
+
+
+# ---------------------------------------------------------------- single-pass FC2 (a research direction)
+
+def fc2_single_pass(d_bf16, w2q_e, k_tile=128):
+    """FC2 of one expert with online amax compensation ("miniTE Technical
+    Report" 5.6, Exploring Single-Pass Fusion), in the pages' order: for each
+    K-tile i of D (the FC1 slice that completes first), the running row amax
+    gamax = max(gamax, max |P_i|); rows with gamax = 0 contribute nothing
+    yet; gs = gamax / 2688; the tile's E4M3 block scales and E2M1 codes are
+    generated with gs (the plain per-token rule with amax = gamax); dO_i is
+    the block-scaled product (block scales included, gs and the weight's
+    outer scale excluded); O = O * (gs_prev / gs) + dO_i; gs_prev = gs.  At
+    the end Y = O * gs_prev * gs_W2 (all-zero rows give zero).
+
+    d_bf16: uint16 [rows, F] (bf16 bits of SwiGLU's output); w2q_e: (codes,
+    sf_lin, scale[1]) of W2_e [H, F].  Returns dict(y (bf16 bits [rows, H]),
+    y_f64 (before rounding), codes, sf (the tiles' codes and block scales side
+    by side, [rows, F/2] and [rows, F/16]), gs_tiles [rows, F/k_tile])."""
+    d = _c(d_bf16, np.uint16)
+    rows, F = d.shape
+    assert F % k_tile == 0 and k_tile % 16 == 0
+    codes_w, sf_w, gs_w = w2q_e
+    b_bs = dequantize(codes_w, sf_w, np.ones(1, np.float32), per_tensor=True)  # q_w s_bw, gs_W2 excluded
+    H = b_bs.shape[0]
+    n_t = F // k_tile
+    gamax = np.zeros(rows, np.float32)
+    gs_prev = np.zeros(rows, np.float64)
+    o = np.zeros((rows, H), np.float64)
+    codes = np.zeros((rows, F // 2), np.uint8)
+    sf = np.zeros((rows, F // 16), np.uint8)
+    gs_tiles = np.zeros((rows, n_t), np.float32)
+    for i in range(n_t):
+        cols = slice(i * k_tile, (i + 1) * k_tile)
+        p = np.ascontiguousarray(d[:, cols])
+        rowmax = np.abs(bf16_to_f64(p)).max(axis=1).astype(np.float32)
+        gamax = np.maximum(gamax, rowmax)
+        live = gamax > 0
+        q_c, q_sf, gs = quantize(p, amax_in=gamax)  # gs = gamax / 2688 in fp32, as the per-token rule
+        codes[:, i * k_tile // 2:(i + 1) * k_tile // 2] = q_c
+        sf[:, i * k_tile // 16:(i + 1) * k_tile // 16] = q_sf
+        gs_tiles[:, i] = gs
+        a_bs = dequantize(q_c, q_sf, np.ones(rows, np.float32))  # q s_b, gs excluded
+        d_o = gemm_f64(a_bs, b_bs[:, cols])
+        g = gs.astype(np.float64)
+        ratio = np.where(live, gs_prev / np.where(live, g, 1.0), 0.0)
+        o = np.where(live[:, None], o * ratio[:, None] + d_o, o)
+        gs_prev = np.where(live, g, gs_prev)
+    y = o * (gs_prev * np.float64(gs_w[0]))[:, None]
+    return dict(y=bf16_round(y), y_f64=y, codes=codes, sf=sf, gs_tiles=gs_tiles)
 
 
 # ---------------------------------------------------------------- metrics
