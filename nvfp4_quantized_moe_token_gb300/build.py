@@ -13,7 +13,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libnvfp4moe.so")
 SOURCES = ["api.cu", "quantize.cu", "dequantize.cu", "route.cu", "gemm.cu", "combine.cu", "noalloc.cu"]
-HEADERS = ["common.cuh", "kernels.h", os.path.join("..", "..", "include", "nvfp4moe.h")]
+HEADERS = ["common.cuh", "fastdiv.cuh", "route_topk.cuh", "kernels.h", os.path.join("..", "..", "include", "nvfp4moe.h")]
 
 NVCC = os.environ.get("NVCC", shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc")
 FLAGS = [
