@@ -327,7 +327,10 @@ NVFP4_API int moe_expert_forward(const void* x_bf16, int64_t T, int64_t H,
  *   top-8 that is more than 518 tokens.
  *   The first call on each device looks the array's device address up
  *   (cudaGetSymbolAddress) with that device current, so make it before any
- *   stream capture.  Nothing is allocated, by this call or later ones.
+ *   stream capture.  Nothing is allocated, by this call or later ones.  The
+ *   address is kept for the life of the process: do not use this entry
+ *   point after cudaDeviceReset or any other teardown of the device's
+ *   primary context.
  *   All calls on a device share the one array: calls whose work overlaps on
  *   the GPU (different streams without ordering) race and corrupt each
  *   other.  Each call clears the device error word at the start of the
