@@ -30,6 +30,13 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+# The CPU oracle's fp64 GEMMs go through numpy's BLAS: one BLAS thread per
+# calling thread, so that the oracle's single-thread and all-core timings use
+# exactly the threads they report (the all-core figure runs one oracle
+# thread per core; the C oracle and BLAS release the GIL).
+for _v in ("OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
@@ -107,10 +114,13 @@ def barrier(world):
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    """nvidia-smi samples (every 20 ms) of SM clock, power and throttle
+    reasons while running; each sample keeps its host time, so a summary can
+    be taken over one timed window."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 20
 
     def __init__(self, device_index):
         self.idx = device_index
@@ -121,7 +131,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(self.PERIOD_MS)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.reader = threading.Thread(target=self._read, daemon=True)
             self.reader.start()
         except OSError:
@@ -129,26 +139,33 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
 
     def stop(self):
         if self.proc is None:
-            return None
+            return
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.reader.join(timeout=2)
-        sm, mx, reasons = [], [], set()
+
+    def summary(self, t0=None, t1=None):
+        """Median SM clock, max clock, max power and the throttle reasons seen
+        in samples taken in [t0, t1] (host monotonic seconds; all when None)."""
+        sm, mx, pw, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ts, ln in self.lines:
+            if (t0 is not None and ts < t0) or (t1 is not None and ts > t1):
+                continue
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
             try:
                 sm.append(float(f[1]))
                 mx.append(float(f[2]))
+                pw.append(float(f[3]))
             except ValueError:
                 continue
             for n, v in zip(names, f[5:9]):
@@ -157,7 +174,7 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "power_w_max": max(pw), "sample_period_ms": self.PERIOD_MS}
 
 
 # ---------------------------------------------------------------- workload
@@ -187,18 +204,19 @@ def recorded_traffic(stage):
     return rec["dram_read_bytes"] + rec["dram_write_bytes"]
 
 
-def algorithmic(R):
-    """Per-launch algorithmic work of each stage (bytes or flops)."""
+def algorithmic(T_, R):
+    """Per-launch algorithmic work of each stage (bytes or flops) of a layer of
+    T_ tokens and R = T_ k token-expert rows."""
     b16, f32 = 2, 4
     q_row = H // 2 + H // 16 + f32
     return {
         # the router top-k runs in the quantize launch (independent work, one launch)
-        "quantize": ("hbm", T * H * b16 + T * q_row + T * E * f32 + E * f32 + T * K_TOP * 8),
-        "route": ("hbm", T * q_row + R * q_row + R * 8),
+        "quantize": ("hbm", T_ * H * b16 + T_ * q_row + T_ * E * f32 + E * f32 + T_ * K_TOP * 8),
+        "route": ("hbm", T_ * q_row + R * q_row + R * 8),
         "fc1": ("tensor", 2.0 * R * (2 * F) * H),
         "requant": ("hbm", R * F * b16 + R * f32 + R * (F // 2 + F // 16 + f32)),
         "fc2": ("tensor", 2.0 * R * H * F),
-        "combine": ("hbm", R * H * b16 + T * K_TOP * 8 + T * H * b16),
+        "combine": ("hbm", R * H * b16 + T_ * K_TOP * 8 + T_ * H * b16),
     }
 
 
@@ -266,68 +284,70 @@ def run_e2e(args, nv, d, w1q, w2q, ws, world, dev):
                           "while step i computes; timed from the first input copy to the last output copy"}
 
 
-def run_ours(args, rank, world, local):
-    import nvfp4_quantized_moe_token_gb300 as nv
-    dev = torch.device("cuda", local)
-    peaks = {}
+def load_peaks():
     pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(pk):
         with open(pk) as f:
-            peaks = json.load(f)
-    hbm_peak = peaks.get("hbm_gbs", 6800.0)
-    bf16_peak = peaks.get("bf16_tflops", 1900.0)
-    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+            return json.load(f), "measured"
+    return {}, "fallback"
 
-    d = make_inputs()
-    x = torch.from_numpy(d["x"].view(np.int16)).view(torch.bfloat16).to(dev)
-    logits = torch.from_numpy(d["logits"]).to(dev)
-    bias = torch.from_numpy(d["bias"]).to(dev)
-    w1q = nv.quantize_grouped_weights(torch.from_numpy(d["w1"].view(np.int16)).view(torch.bfloat16).to(dev))
-    w2q = nv.quantize_grouped_weights(torch.from_numpy(d["w2"].view(np.int16)).view(torch.bfloat16).to(dev))
-    need = nv.lib().moe_expert_workspace(T, H, F, E, K_TOP)
-    ws = torch.zeros(need, dtype=torch.uint8, device=dev)
-    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-    flush = L2Flush(dev)
-    stream = torch.cuda.current_stream(dev)
-    R = T * K_TOP
 
-    def step(evs=None):
-        nv.moe_expert_forward(x, logits, bias, w1q, w2q, F, K_TOP, out=out, ws=ws, stage_events=evs)
+class Layer:
+    """One expert layer's device inputs, pre-quantized weights, workspace and
+    output, and the call that runs it."""
 
-    for _ in range(max(args.warmup, 3)):
-        step()
+    def __init__(self, nv, dev, d):
+        self.nv = nv
+        self.d = d
+        self.T = d["x"].shape[0]
+        self.x = torch.from_numpy(d["x"].view(np.int16)).view(torch.bfloat16).to(dev)
+        self.logits = torch.from_numpy(d["logits"]).to(dev)
+        self.bias = torch.from_numpy(d["bias"]).to(dev)
+        self.w1q = nv.quantize_grouped_weights(torch.from_numpy(d["w1"].view(np.int16)).view(torch.bfloat16).to(dev))
+        self.w2q = nv.quantize_grouped_weights(torch.from_numpy(d["w2"].view(np.int16)).view(torch.bfloat16).to(dev))
+        self.ws = torch.zeros(nv.lib().moe_expert_workspace(self.T, H, F, E, K_TOP), dtype=torch.uint8, device=dev)
+        self.out = torch.empty((self.T, H), dtype=torch.bfloat16, device=dev)
+
+    def __call__(self, evs=None):
+        self.nv.moe_expert_forward(self.x, self.logits, self.bias, self.w1q, self.w2q, F, K_TOP, out=self.out,
+                                   ws=self.ws, stage_events=evs)
+
+    def check_error_word(self):
+        err = self.ws[:4].view(torch.int32).item()
+        if err != 0:
+            raise RuntimeError(f"device error word {err:#x}")
+
+
+def time_layer(layer, steps, warmup, flush, world, dev):
+    """Mean step time and per-stage times (library stage events) of `steps`
+    steps, L2 flushed before each step outside its events; also returns the
+    host-time window of the timed loop."""
+    nv = layer.nv
+    for _ in range(max(warmup, 3)):
+        layer()
     torch.cuda.synchronize()
-    err = ws[:4].view(torch.int32).item()
-    if err != 0:
-        raise RuntimeError(f"device error word {err:#x}")
-
-    clocks = ClockSampler(local) if not args.quick else None
-    if clocks:
-        clocks.start()
-        time.sleep(0.3)
+    layer.check_error_word()
     nev = len(nv.STAGES) + 1
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(steps)]
     barrier(world)
     torch.cuda.synchronize()
+    t0 = time.monotonic()
     torch.cuda.nvtx.range_push("timed")
-    for i in range(args.steps):
+    for i in range(steps):
         flush()
-        step(events[i])
+        layer(events[i])
     torch.cuda.synchronize()
     torch.cuda.nvtx.range_pop()
+    t1 = time.monotonic()
     barrier(world)
+    layer.check_error_word()
     step_ms = [ev[0].elapsed_time(ev[-1]) for ev in events]
     stage_ms = {s: [ev[j].elapsed_time(ev[j + 1]) for ev in events] for j, s in enumerate(nv.STAGES)}
-    mean_ms = statistics.fmean(step_ms)
-    mean_ms_all = reduce_max(mean_ms, world, dev)
+    return statistics.fmean(step_ms), stage_ms, (t0, t1), min(step_ms)
 
-    e2e = None
-    if not (args.no_e2e or args.quick):
-        e2e = run_e2e(args, nv, d, w1q, w2q, ws, world, dev)
-    clk = clocks.stop() if clocks else None
 
-    # per-stage rooflines, dominant stage first
-    alg = algorithmic(R)
+def stage_rooflines(nv, T_, stage_ms, mean_ms, hbm_peak, bf16_peak):
+    alg = algorithmic(T_, T_ * K_TOP)
     stages = {}
     for s in nv.STAGES:
         ms = statistics.fmean(stage_ms[s])
@@ -342,6 +362,83 @@ def run_ours(args, rank, world, local):
             ach = work / (ms / 1e3) / 1e9
             stages[s] = {"ms": ms, "share": ms / mean_ms, "bound": "hbm", "achieved": ach, "unit": "GB/s",
                          "peak": hbm_peak, "frac": ach / hbm_peak}
+    gemm_ms = stages["fc1"]["ms"] + stages["fc2"]["ms"]
+    gemm_flop = alg["fc1"][1] + alg["fc2"][1]
+    gemms = {"ms": gemm_ms, "tflops": gemm_flop / (gemm_ms / 1e3) / 1e12,
+             "frac_of_9pf": gemm_flop / (gemm_ms / 1e3) / 1e12 / 9000.0,
+             "frac": gemm_flop / (gemm_ms / 1e3) / 1e12 / (bf16_peak * FP4_OVER_BF16)}
+    return stages, gemms, alg
+
+
+def sustained_leg(layer, local, seconds=2.5):
+    """The layer back to back (no L2 flush) for about `seconds`, with SM clocks
+    sampled inside that loop only: the rate a long run settles at under the
+    power cap.  Stage events on every 16th step give the GEMMs' sustained rate."""
+    nv = layer.nv
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(20):
+        layer()
+    b.record()
+    torch.cuda.synchronize()
+    n = max(int(seconds * 1e3 / (a.elapsed_time(b) / 20)), 100)
+    nev = len(nv.STAGES) + 1
+    sampled = {i: [torch.cuda.Event(enable_timing=True) for _ in range(nev)] for i in range(0, n, 16)}
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.2)
+    torch.cuda.synchronize()
+    t0 = time.monotonic()
+    a.record()
+    for i in range(n):
+        layer(sampled.get(i))
+    b.record()
+    torch.cuda.synchronize()
+    t1 = time.monotonic()
+    clocks.stop()
+    layer.check_error_word()
+    ms = a.elapsed_time(b) / n
+    clk = clocks.summary(t0, t1)
+    fc = {s: statistics.fmean(ev[j].elapsed_time(ev[j + 1]) for ev in sampled.values())
+          for j, s in enumerate(nv.STAGES) if s in ("fc1", "fc2")}
+    R = layer.T * K_TOP
+    gemm_flop = 2.0 * R * (2 * F) * H + 2.0 * R * H * F
+    out = {"seconds": ms * n / 1e3, "steps": n, "ms_per_step": ms, "tokens_per_s": layer.T / (ms / 1e3),
+           "fc1_ms": fc["fc1"], "fc2_ms": fc["fc2"],
+           "gemm_tflops": gemm_flop / ((fc["fc1"] + fc["fc2"]) / 1e3) / 1e12, "clocks": clk}
+    if clk:
+        out["ms_x_median_sm_mhz"] = ms * clk["sm_mhz"]
+    return out
+
+
+def run_ours(args, rank, world, local):
+    import nvfp4_quantized_moe_token_gb300 as nv
+    dev = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+    hbm_peak = peaks.get("hbm_gbs", 6800.0)
+    bf16_peak = peaks.get("bf16_tflops", 1900.0)
+
+    d = make_inputs()
+    layer = Layer(nv, dev, d)
+    flush = L2Flush(dev)
+    clocks = ClockSampler(local) if not args.quick else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    mean_ms, stage_ms, window, min_ms = time_layer(layer, args.steps, args.warmup, flush, world, dev)
+    mean_ms_all = reduce_max(mean_ms, world, dev)
+
+    e2e = None
+    if not (args.no_e2e or args.quick):
+        e2e = run_e2e(args, nv, d, layer.w1q, layer.w2q, layer.ws, world, dev)
+    if clocks:
+        clocks.stop()
+    clk = clocks.summary() if clocks else None
+    if clk:
+        inside = clocks.summary(*window)
+        clk["timed_region"] = inside if inside else {"samples": 0, "note": "the timed loop ended between samples"}
+
+    stages, gemms, alg = stage_rooflines(nv, T, stage_ms, mean_ms, hbm_peak, bf16_peak)
     dom = max(stages, key=lambda s: stages[s]["ms"])
     dm = stages[dom]
     roofline = {"kernel": dom, "bound": dm["bound"], "achieved": dm["achieved"], "peak": dm["peak"],
@@ -354,11 +451,27 @@ def run_ours(args, rank, world, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms_all, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e2m1 x e4m3 -> f32 acc, bf16 io", "data": "synthetic",
         "config": dict(CONFIG, parallelism=f"replicas x{world}"),
-        "e2e": e2e, "roofline": roofline, "stages": stages,
+        "e2e": e2e, "roofline": roofline, "stages": stages, "gemms_fc1_fc2": gemms,
+        "ms_per_step_min": min_ms,
         "gpu_launches": 8 * args.steps,
         "clocks": clk,
     }
-    return res, d
+    return res, d, layer
+
+
+def moe_8k_leg(nv, local, steps, warmup):
+    """The 8192-token layer (router bias ~N(0, 1)), timed like the headline one."""
+    dev = torch.device("cuda", local)
+    peaks, _ = load_peaks()
+    layer = Layer(nv, dev, workloads.moe_8k())
+    mean_ms, stage_ms, _, min_ms = time_layer(layer, steps, warmup, L2Flush(dev), 1, dev)
+    stages, gemms, _ = stage_rooflines(nv, layer.T, stage_ms, mean_ms, peaks.get("hbm_gbs", 6800.0),
+                                       peaks.get("bf16_tflops", 1900.0))
+    del layer
+    torch.cuda.empty_cache()
+    return {"workload": "moe_expert_layer_8k (8192 tokens, router bias std 1, seed 2)", "ms_per_step": mean_ms,
+            "ms_per_step_min": min_ms, "tokens_per_s": 8192 / (mean_ms / 1e3), "steps": steps,
+            "gemms_fc1_fc2": gemms, "stages": stages}
 
 
 def _graph_per_launch(calls, replays, dev):
@@ -641,41 +754,163 @@ def cpu_threads():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(d, budget_s=10.0, sample=64):
-    w1q, w2q, wdeq = oracle_setup(d)
-    n_tok, t0 = 0, time.perf_counter()
-    while time.perf_counter() - t0 < budget_s:
-        oracle_sample_tokens(d, w1q, w2q, wdeq, (n_tok * 7) % (T - sample), sample)
-        n_tok += sample
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for ln in r.stdout.splitlines():
+            if ln.strip().startswith("Model name:"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.TimeoutExpired):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith(("model name", "cpu part")):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def oracle_tokens_per_s(d, w1q, w2q, wdeq, threads, budget_s, sample):
+    """Tokens/s of the oracle layer over `budget_s` seconds on `threads` host
+    threads (one BLAS thread each), each running its own batches of `sample`
+    consecutive tokens."""
+    import concurrent.futures as cf
+    t0 = time.perf_counter()
+
+    def worker(w):
+        n, i = 0, 0
+        while time.perf_counter() - t0 < budget_s:
+            start = ((w * 9973 + i * threads * 7) * sample) % (T - sample)
+            oracle_sample_tokens(d, w1q, w2q, wdeq, start, sample)
+            n += sample
+            i += 1
+        return n
+
+    with cf.ThreadPoolExecutor(threads) as ex:
+        n_tok = sum(ex.map(worker, range(threads)))
     dt = time.perf_counter() - t0
-    return {"value": n_tok / dt, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
-            "sample": f"{n_tok} tokens of the 32768-token layer in batches of {sample} "
-                      f"(full route/quantize/permute/FC1/SwiGLU/requant/FC2/combine per batch, fp64 GEMMs "
-                      f"via numpy BLAS, weights pre-quantized), {dt:.1f} s"}
+    return n_tok / dt, n_tok, dt
+
+
+def cpu_baseline(d, budget_s=8.0, sample=64):
+    """The oracle on the host's cores: once on one thread, once on every core
+    (one oracle thread per core), BLAS pinned to one thread per caller."""
+    w1q, w2q, wdeq = oracle_setup(d)
+    n_cores = cpu_threads()
+    v1, n1, dt1 = oracle_tokens_per_s(d, w1q, w2q, wdeq, 1, budget_s, sample)
+    vn, nn, dtn = oracle_tokens_per_s(d, w1q, w2q, wdeq, n_cores, budget_s, sample)
+    return {"value": vn, "unit": "tokens/s", "cores": n_cores, "kind": "oracle",
+            "sample": f"{nn} tokens of the 32768-token layer in batches of {sample} consecutive tokens on "
+                      f"{n_cores} threads, {dtn:.1f} s (full route/quantize/permute/FC1/SwiGLU/requant/FC2/"
+                      f"combine per batch; fp64 GEMMs by numpy BLAS, one BLAS thread per oracle thread; weights "
+                      f"quantized and dequantized once)",
+            "single_thread": {"value": v1, "unit": "tokens/s", "cores": 1,
+                              "sample": f"{n1} tokens in batches of {sample}, {dt1:.1f} s"},
+            "cpu_model": cpu_model(), "blas_threads_per_worker": 1}
+
+
+def cpu_configs():
+    """The oracle, single-threaded, on the other workloads: the 64 x 256 x 512
+    linear and the 16384 x 2048 quantization in full, the attention
+    projections' quantization in full and their fp64 GEMM on a 256-row sample,
+    and the 8192-token layer's routing and quantization in full."""
+    import oracle
+    out = {}
+    lin = workloads.linear_small()
+    t0 = time.perf_counter()
+    oracle.linear(oracle.quantize(lin["x"]), oracle.quantize(lin["w"], per_tensor=True))
+    out["linear_64x256x512"] = {"s": time.perf_counter() - t0, "scope": "full"}
+    q = workloads.quant_rows()["x"]
+    t0 = time.perf_counter()
+    oracle.quantize(q)
+    dt = time.perf_counter() - t0
+    out["quantize_16384x2048"] = {"s": dt, "gbs": 16384 * (2048 * 2 + 1024 + 128 + 4) / dt / 1e9, "scope": "full"}
+    del q
+    ap = workloads.attn_proj()
+    for name, xk, wk in (("qkv_proj", "x", "wqkv"), ("o_proj", "o", "wo")):
+        t0 = time.perf_counter()
+        xq = oracle.quantize(ap[xk])
+        tq = time.perf_counter() - t0
+        wq = oracle.quantize(ap[wk], per_tensor=True)
+        rows = slice(0, 256)
+        t0 = time.perf_counter()
+        oracle.linear((xq[0][rows], xq[1][rows], xq[2][rows]), wq)
+        tg = time.perf_counter() - t0
+        M, K = ap[xk].shape
+        N = ap[wk].shape[0]
+        out[name] = {"quantize_s_full": tq, "gemm_s_256_rows": tg,
+                     "gemm_s_full_extrapolated": tg * M / 256, "gflops": 2.0 * 256 * N * K / tg / 1e9}
+    del ap
+    m8 = workloads.moe_8k(with_weights=False)
+    t0 = time.perf_counter()
+    ids, _ = oracle.route(m8["logits"], m8["bias"], K_TOP)
+    oracle.route_metadata(ids, E)
+    tr = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle.quantize(m8["x"])
+    out["moe_8k_route_and_quantize"] = {"route_s": tr, "quantize_s": time.perf_counter() - t0, "scope": "full"}
+    return {"threads": 1, "results": out}
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return
+    import concurrent.futures as cf
     d = make_inputs()
     w1q, w2q, wdeq = oracle_setup(d)
-    sample = 16
+    n_cores = cpu_threads()
+    sample = 8  # tokens per oracle thread per step: a step is n_cores x 8 tokens
     for i in range(args.warmup):
         oracle_sample_tokens(d, w1q, w2q, wdeq, i * sample, sample)
     t0 = time.perf_counter()
-    for i in range(args.steps):
-        oracle_sample_tokens(d, w1q, w2q, wdeq, (i * sample * 13) % (T - sample), sample)
+    with cf.ThreadPoolExecutor(n_cores) as ex:
+        for i in range(args.steps):
+            list(ex.map(lambda w: oracle_sample_tokens(d, w1q, w2q, wdeq,
+                                                       ((i * n_cores + w) * sample * 13) % (T - sample), sample),
+                        range(n_cores)))
     dt = time.perf_counter() - t0
-    value = args.steps * sample / dt
+    value = args.steps * n_cores * sample / dt
     res = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
            "data": "synthetic", "config": dict(CONFIG, parallelism="host cores"),
-           "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
-                            "sample": f"each step: {sample} tokens of the 32768-token layer through the CPU "
-                                      f"oracle (weights pre-quantized)"},
+           "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": n_cores, "kind": "oracle",
+                            "sample": f"each step: {n_cores} oracle threads (one BLAS thread each) x {sample} "
+                                      f"tokens of the 32768-token layer (weights quantized once)",
+                            "cpu_model": cpu_model()},
            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(res))
+
+
+def summary_of(res):
+    """The figures a reader looks for first, last on the line (a truncated
+    tail of the output still shows them)."""
+    st = res["stages"]
+    out = {"moe_32k_tokens_per_s": res["value"], "moe_32k_ms": res["ms_per_step"],
+           "fc1_ms": st["fc1"]["ms"], "fc2_ms": st["fc2"]["ms"],
+           "fc1_plus_fc2_ms": res["gemms_fc1_fc2"]["ms"],
+           "fc1_plus_fc2_frac_of_9pf": res["gemms_fc1_fc2"]["frac_of_9pf"]}
+    if res.get("e2e"):
+        out["e2e_tokens_per_s"] = res["e2e"]["value"]
+    if res.get("moe_8k"):
+        out["moe_8k_tokens_per_s"] = res["moe_8k"]["tokens_per_s"]
+        out["moe_8k_fc1_plus_fc2_frac_of_9pf"] = res["moe_8k"]["gemms_fc1_fc2"]["frac_of_9pf"]
+    if res.get("sustained"):
+        su = res["sustained"]
+        out["sustained_tokens_per_s"] = su["tokens_per_s"]
+        out["sustained_sm_mhz"] = (su.get("clocks") or {}).get("sm_mhz")
+    if res.get("quant"):
+        out["quant_us"] = res["quant"]["us"]
+        out["quant_frac_of_hbm"] = res["quant"]["frac_of_hbm"]
+    if res.get("quant_four_over_six"):
+        out["quant_46_frac_of_hbm"] = res["quant_four_over_six"]["frac_of_hbm"]
+    if res.get("cpu_baseline"):
+        out["cpu_oracle_tokens_per_s_all_cores"] = res["cpu_baseline"]["value"]
+        out["cpu_oracle_tokens_per_s_1_thread"] = res["cpu_baseline"]["single_thread"]["value"]
+    return out
 
 
 def main():
@@ -691,9 +926,13 @@ def main():
             fn = quant_gbs if args.only == "quant" else dequant_gbs
             print(json.dumps({args.only: fn(args, local, reps=max(args.steps, 1))}))
         return
-    res, d = run_ours(args, rank, world, local)
+    res, d, layer = run_ours(args, rank, world, local)
     if rank == 0:
         if not args.quick:
+            res["sustained"] = sustained_leg(layer, local)
+            del layer
+            torch.cuda.empty_cache()
+            res["moe_8k"] = moe_8k_leg(nv, local, args.steps, args.warmup)
             res["quant"] = quant_gbs(args, local)
             res["quant_four_over_six"] = quant_gbs(args, local, four_over_six="mse")
             res["dequant"] = dequant_gbs(args, local)
@@ -702,6 +941,9 @@ def main():
             res["library_fp4_reference"] = library_fp4_reference(local)
         if not (args.no_cpu_baseline or args.quick):
             res["cpu_baseline"] = cpu_baseline(d)
+            res["cpu_oracle_configs"] = cpu_configs()
+        if not args.quick:
+            res["summary"] = summary_of(res)
         print(json.dumps(res))
     if world > 1:
         import torch.distributed as dist
