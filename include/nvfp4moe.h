@@ -77,10 +77,13 @@ extern "C" {
  * and Activations); see nvfp4_quantize_rows. */
 #define NVFP4_FOUR_OVER_SIX_MSE 2 /* error = sum of squared differences */
 #define NVFP4_FOUR_OVER_SIX_MAE 4 /* error = sum of absolute differences */
+/* nvfp4_dequantize_rows only: write row r at its padded row (see there). */
+#define NVFP4_DQ_PADDED_ROWS 8
 
 /* Bits of the device error word. */
 #define NVFP4_DEVERR_TIMEOUT 1u   /* a pipeline wait (GEMM or quantizer) ran past its limit */
 #define NVFP4_DEVERR_BADEXPERT 2u /* a routed expert id outside [0, E) */
+#define NVFP4_DEVERR_BADGROUP 4u  /* grouped BF16 GEMM: padded offsets not ascending multiples of 128 */
 
 /*
  * An NVFP4 matrix [rows x cols] in device memory (caller-owned):
@@ -177,21 +180,64 @@ NVFP4_API int nvfp4_quantize_grouped(const void* x_bf16, int groups, int64_t row
  * quantization decisions (the pages' "Improving Gradient Stability":
  * dequantized backward for weights and activations; decode as "miniTE
  * Technical Report" 2.2).  s_g = in->scale[r] (NVFP4_PER_ROW) or
- * in->scale[0] (NVFP4_PER_TENSOR); four-over-six flags are ignored (the
- * decode rule is the same).
+ * in->scale[0] (NVFP4_PER_TENSOR; with group offsets, in->scale[g] for the
+ * rows of group g: the stacked per-expert weights of nvfp4_quantize_grouped);
+ * four-over-six flags are ignored (the decode rule is the same).
  * group_offsets / padded_offsets (nullable, device, [groups + 1]): the block
  * scales of row r live at padded row padded_offsets[g] + (r -
  * group_offsets[g]) for the group g holding r, as in the expert-ordered
  * buffers of moe_expert_forward (a1, a2); NULL = scale row r.
- * y is bf16 [rows x cols], row stride ldy elements.
+ * y is bf16 [rows x cols], row stride ldy elements.  With NVFP4_DQ_PADDED_ROWS
+ * (offsets required) y follows the padded layout as well: row r goes to the
+ * padded row above, and the padding rows of every group (padded_offsets[g] +
+ * count .. padded_offsets[g + 1]) are written with zeros, so y must hold
+ * padded_offsets[groups] rows: the operand layout of the grouped BF16 GEMMs.
  * Shapes: rows >= 0, 0 < cols <= 32768, cols % 16 == 0, ldy >= cols,
  *         ldy % 8 == 0; 1 <= groups <= 256 when offsets are given.
- *         rows == 0 is a no-op (the buffers may then be null).
+ *         rows == 0 is a no-op (the buffers may then be null); with
+ *         NVFP4_DQ_PADDED_ROWS it writes only the zero padding rows.
  * Alignment: codes 16-byte aligned, y 16-byte aligned, scale 4-byte aligned.
  */
 NVFP4_API int nvfp4_dequantize_rows(const nvfp4_tensor* in, int scale_mode, const int* group_offsets,
                                     const int* padded_offsets, int groups, void* y_bf16, int64_t ldy,
                                     void* stream);
+
+/*
+ * Grouped BF16 GEMMs of the dequantized backward (the pages' "Improving
+ * Gradient Stability": the backward of y = DQ(Q(x)) . DQ(Q(w))^T runs on the
+ * BF16 dequantized operands x^ = DQ(Q(x)) and w^ = DQ(Q(w)) of the exact
+ * tensors the forward pass used; "miniTE Technical Report" 4.2: BF16
+ * backward GEMMs).  tcgen05 kind::f16 on the tensor cores, fp32
+ * accumulation, bf16 results rounded once to nearest even.
+ *
+ * Rows are grouped by padded_offsets (device, [groups + 1], ascending
+ * multiples of 128: the 128-row-padded expert layout of moe_expert_forward's
+ * scale buffers, which nvfp4_dequantize_rows with NVFP4_DQ_PADDED_ROWS
+ * writes; the padding rows must hold zeros), or, with padded_offsets NULL,
+ * form one group of `rows` rows (any count: the dense linear).  Offsets that
+ * are not ascending multiples of 128 within `rows` set NVFP4_DEVERR_BADGROUP
+ * in the error word and nothing is written.
+ *
+ * nvfp4_grouped_dgrad_bf16: for each group g and each of its rows r,
+ *   dx[r][k] = sum_n dy[r][n] * w[g][n][k]
+ * dy bf16 [rows x nf], w bf16 [groups x nf x kf] (each expert's DQ(Q(W)) in
+ * its forward layout [N x K], stacked), dx bf16 [rows x kf]; all row-major,
+ * contiguous.  dx rows of the padding rows are written (zero, as dy's are).
+ * nvfp4_grouped_wgrad_bf16: for each group g,
+ *   dw[g][n][k] = sum over the rows r of g of dy[r][n] * x[r][k]
+ * dy bf16 [rows x nf], x bf16 [rows x kf], dw bf16 [groups x nf x kf]; a
+ * group with no rows gets a zero dw[g].
+ * Shapes: rows >= 0; kf % 256 == 0; nf % 64 == 0 (dgrad) or nf % 256 == 0
+ *         (wgrad); 1 <= groups <= 256 with offsets.
+ * Alignment: every operand 16-byte aligned.
+ * ws: nullable; when ws_bytes >= 4 its first uint32 is the device error word.
+ */
+NVFP4_API int nvfp4_grouped_dgrad_bf16(const void* dy_bf16, const void* w_bf16, void* dx_bf16, int64_t rows,
+                                       int64_t nf, int64_t kf, const int* padded_offsets, int groups, void* ws,
+                                       size_t ws_bytes, void* stream);
+NVFP4_API int nvfp4_grouped_wgrad_bf16(const void* dy_bf16, const void* x_bf16, void* dw_bf16, int64_t rows,
+                                       int64_t nf, int64_t kf, const int* padded_offsets, int groups, void* ws,
+                                       size_t ws_bytes, void* stream);
 
 /*
  * nvfp4_linear: y[m][n] = bf16( s_gx[m] * s_gw * sum_k (q_x s_bx)(q_w s_bw) )

@@ -46,12 +46,14 @@ class _Layout(ctypes.Structure):
 
 PER_ROW = 0
 PER_TENSOR = 1
+DQ_PADDED_ROWS = 8    # nvfp4_dequantize_rows: rows written at their padded positions
 DEVERR_TIMEOUT = 1    # bits of the device error word
 DEVERR_BADEXPERT = 2
+DEVERR_BADGROUP = 4
 FOUR_OVER_SIX = {None: 0, "mse": 2, "mae": 4}  # scale-mode flags of four-over-six block scaling
 SYMBOLS = ["nvfp4_sf_bytes", "nvfp4_quantize_workspace", "nvfp4_quantize_rows", "nvfp4_quantize_grouped",
            "nvfp4_dequantize_rows",
-           "nvfp4_linear",
+           "nvfp4_linear", "nvfp4_grouped_dgrad_bf16", "nvfp4_grouped_wgrad_bf16",
            "moe_expert_workspace_layout", "moe_expert_workspace", "moe_expert_forward",
            "moe_expert_forward_noalloc", "nvfp4_last_error"]
 
@@ -86,6 +88,9 @@ def lib():
         L.nvfp4_dequantize_rows.restype = ctypes.c_int
         L.nvfp4_dequantize_rows.argtypes = [ctypes.POINTER(_Tensor), ctypes.c_int, c_vp, c_vp, ctypes.c_int, c_vp,
                                             c_i64, c_vp]
+        for fn in (L.nvfp4_grouped_dgrad_bf16, L.nvfp4_grouped_wgrad_bf16):
+            fn.restype = ctypes.c_int
+            fn.argtypes = [c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_vp, ctypes.c_int, c_vp, ctypes.c_size_t, c_vp]
         L.nvfp4_linear.restype = ctypes.c_int
         L.nvfp4_linear.argtypes = [ctypes.POINTER(_Tensor), ctypes.POINTER(_Tensor), c_vp, c_i64,
                                    c_vp, ctypes.c_size_t, c_vp]
@@ -162,19 +167,56 @@ def quantize_rows(x, per_tensor=False, amax_in=None, out=None, four_over_six=Non
     return out
 
 
-def dequantize_rows(t, per_tensor=False, group_offsets=None, padded_offsets=None, out=None, stream=None):
+def dequantize_rows(t, per_tensor=False, group_offsets=None, padded_offsets=None, out=None, padded_rows=False,
+                    stream=None):
     """NVFP4Tensor -> bf16 [rows, cols] = bf16(q s_b s_g), the exact product rounded
     once (DQ(Q(x)), the BF16 backward operand).  group_offsets / padded_offsets
     (int32 CUDA tensors [G+1]): scale rows padded per group, as in the expert-ordered
-    buffers of moe_expert_forward."""
+    buffers of moe_expert_forward; per_tensor with offsets takes one scale per group.
+    padded_rows: rows written at their padded positions, padding rows zeroed (out
+    must then hold padded_offsets[G] rows)."""
     if out is None:
+        assert not padded_rows, "padded_rows needs an out buffer of padded_offsets[G] rows"
         out = torch.empty((t.rows, t.cols), dtype=torch.bfloat16, device=t.codes.device)
     assert out.dtype == torch.bfloat16 and out.stride(1) == 1
     G = 0 if group_offsets is None else group_offsets.numel() - 1
-    rc = lib().nvfp4_dequantize_rows(ctypes.byref(t.c()), PER_TENSOR if per_tensor else PER_ROW,
+    mode = (PER_TENSOR if per_tensor else PER_ROW) | (DQ_PADDED_ROWS if padded_rows else 0)
+    rc = lib().nvfp4_dequantize_rows(ctypes.byref(t.c()), mode,
                                      _ptr(group_offsets), _ptr(padded_offsets), G, _ptr(out), out.stride(0),
                                      _stream(stream))
     _check(rc, "nvfp4_dequantize_rows")
+    return out
+
+
+def grouped_dgrad_bf16(dy, w, padded_offsets=None, out=None, err=None, stream=None):
+    """dx = dy . w_g per row group: dy bf16 [rows, nf], w bf16 [G, nf, kf] (each
+    group's DQ(Q(W)) in its forward layout), padded_offsets int32 [G+1] (ascending
+    multiples of 128) or None for one dense group; returns dx bf16 [rows, kf]."""
+    rows, nf = dy.shape
+    G, nf2, kf = w.shape
+    assert nf2 == nf and dy.is_contiguous() and w.is_contiguous()
+    if out is None:
+        out = torch.empty((rows, kf), dtype=torch.bfloat16, device=dy.device)
+    rc = lib().nvfp4_grouped_dgrad_bf16(_ptr(dy), _ptr(w), _ptr(out), rows, nf, kf, _ptr(padded_offsets),
+                                        G if padded_offsets is not None else 1, _ptr(err),
+                                        0 if err is None else err.numel() * err.element_size(), _stream(stream))
+    _check(rc, "nvfp4_grouped_dgrad_bf16")
+    return out
+
+
+def grouped_wgrad_bf16(dy, x, padded_offsets=None, groups=1, out=None, err=None, stream=None):
+    """dw_g = dy[rows of g]^T . x[rows of g]: dy bf16 [rows, nf], x bf16 [rows, kf],
+    padded_offsets int32 [G+1] or None (one group); returns dw bf16 [G, nf, kf]."""
+    rows, nf = dy.shape
+    rows2, kf = x.shape
+    assert rows2 == rows and dy.is_contiguous() and x.is_contiguous()
+    G = padded_offsets.numel() - 1 if padded_offsets is not None else 1
+    if out is None:
+        out = torch.empty((G, nf, kf), dtype=torch.bfloat16, device=dy.device)
+    rc = lib().nvfp4_grouped_wgrad_bf16(_ptr(dy), _ptr(x), _ptr(out), rows, nf, kf, _ptr(padded_offsets), G,
+                                        _ptr(err), 0 if err is None else err.numel() * err.element_size(),
+                                        _stream(stream))
+    _check(rc, "nvfp4_grouped_wgrad_bf16")
     return out
 
 

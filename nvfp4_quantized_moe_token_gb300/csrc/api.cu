@@ -160,12 +160,18 @@ int nvfp4_quantize_grouped(const void* x_bf16, int groups, int64_t rows_per_grou
 
 int nvfp4_dequantize_rows(const nvfp4_tensor* in, int scale_mode, const int* group_offsets,
                           const int* padded_offsets, int groups, void* y_bf16, int64_t ldy, void* stream) {
-    if (in != nullptr && in->rows == 0 && in->cols > 0 && in->cols % 16 == 0) return ok();  // nothing to write
-    int rc = check_tensor(in, "dequantize in");
+    const bool padded_rows = (scale_mode & NVFP4_DQ_PADDED_ROWS) != 0;
+    if (in != nullptr && in->rows == 0 && !padded_rows && in->cols > 0 && in->cols % 16 == 0)
+        return ok();  // nothing to write
+    // with no data rows the input buffers are never read (a padded layout then gets only its zero rows)
+    int rc = (in != nullptr && in->rows == 0) ? NVFP4_OK : check_tensor(in, "dequantize in");
     if (rc) return rc;
+    if (in == nullptr || in->cols <= 0) return fail(NVFP4_EINVAL, "dequantize: null input or bad cols");
     if (y_bf16 == nullptr) return fail(NVFP4_EINVAL, "dequantize: y is null");
-    if (!fos_flags_valid(scale_mode & ~NVFP4_PER_TENSOR))
+    if (!fos_flags_valid(scale_mode & ~(NVFP4_PER_TENSOR | NVFP4_DQ_PADDED_ROWS)))
         return fail(NVFP4_EINVAL, "dequantize: unknown scale_mode %d", scale_mode);
+    if (padded_rows && group_offsets == nullptr)
+        return fail(NVFP4_EINVAL, "dequantize: NVFP4_DQ_PADDED_ROWS needs group and padded offsets");
     const int64_t rows = in->rows, cols = in->cols;
     if (cols % 16 != 0) return fail(NVFP4_ESHAPE, "dequantize: cols %% 16 != 0 (cols = %lld)", (long long)cols);
     if (rows >= (1ll << 31) || cols > 32768) return fail(NVFP4_ESHAPE, "dequantize: rows >= 2^31 or cols > 32768");
@@ -185,6 +191,7 @@ int nvfp4_dequantize_rows(const nvfp4_tensor* in, int scale_mode, const int* gro
     d.goff = group_offsets;
     d.gpoff = padded_offsets;
     d.G = group_offsets != nullptr ? groups : 0;
+    d.padded_rows = padded_rows ? 1 : 0;
     d.y = y_bf16;
     d.ldy = ldy;
     cudaError_t e = nvfp4::launch_dequantize(d, reinterpret_cast<cudaStream_t>(stream));
@@ -228,6 +235,73 @@ int nvfp4_linear(const nvfp4_tensor* x, const nvfp4_tensor* w, void* y_bf16, int
     g.num_sms = sm_count();
     cudaError_t e = nvfp4::launch_gemm(g, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(NVFP4_ELAUNCH, "linear: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+namespace {
+// Shared argument checks of the two grouped BF16 GEMMs.
+int bwd_check(const char* name, const void* a, const void* b, const void* c, int64_t rows, int64_t nf, int64_t kf,
+              const int* padded_offsets, int groups, void* ws, size_t ws_bytes, bool wgrad) {
+    if (a == nullptr || b == nullptr || c == nullptr) return fail(NVFP4_EINVAL, "%s: null operand", name);
+    if (rows < 0 || rows >= (1ll << 31)) return fail(NVFP4_ESHAPE, "%s: rows must be in [0, 2^31)", name);
+    if (nf <= 0 || kf <= 0 || nf >= (1 << 24) || kf >= (1 << 24))
+        return fail(NVFP4_ESHAPE, "%s: bad nf / kf", name);
+    if (kf % 256 != 0) return fail(NVFP4_ESHAPE, "%s: kf %% 256 != 0 (kf = %lld)", name, (long long)kf);
+    if (wgrad ? nf % 256 != 0 : nf % 64 != 0)
+        return fail(NVFP4_ESHAPE, "%s: nf must be a multiple of %d (nf = %lld)", name, wgrad ? 256 : 64,
+                    (long long)nf);
+    if (padded_offsets != nullptr && (groups < 1 || groups > 256))
+        return fail(NVFP4_ESHAPE, "%s: groups must be in [1, 256]", name);
+    if (padded_offsets != nullptr && !aligned(padded_offsets, 4)) return fail(NVFP4_EALIGN, "%s: offsets misaligned", name);
+    if (!aligned(a, 16) || !aligned(b, 16) || !aligned(c, 16))
+        return fail(NVFP4_EALIGN, "%s: operands must be 16-byte aligned", name);
+    if (ws != nullptr && ws_bytes >= 4 && !aligned(ws, 4)) return fail(NVFP4_EALIGN, "%s: ws misaligned", name);
+    if (sm_count() <= 0) return fail(NVFP4_ELAUNCH, "%s: no CUDA device", name);
+    return NVFP4_OK;
+}
+}  // namespace
+
+int nvfp4_grouped_dgrad_bf16(const void* dy_bf16, const void* w_bf16, void* dx_bf16, int64_t rows, int64_t nf,
+                             int64_t kf, const int* padded_offsets, int groups, void* ws, size_t ws_bytes,
+                             void* stream) {
+    int rc = bwd_check("dgrad", dy_bf16, w_bf16, dx_bf16, rows, nf, kf, padded_offsets, groups, ws, ws_bytes, false);
+    if (rc) return rc;
+    nvfp4::GemmBf16Launch g{};
+    g.wgrad = 0;
+    g.dy = dy_bf16;
+    g.w = w_bf16;
+    g.out = dx_bf16;
+    g.rows = rows;
+    g.nf = (int)nf;
+    g.kf = (int)kf;
+    g.gpoff = padded_offsets;
+    g.G = padded_offsets ? groups : 1;
+    g.err = (ws != nullptr && ws_bytes >= 4) ? reinterpret_cast<uint32_t*>(ws) : nullptr;
+    g.num_sms = sm_count();
+    cudaError_t e = nvfp4::launch_gemm_bf16(g, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(NVFP4_ELAUNCH, "dgrad: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+int nvfp4_grouped_wgrad_bf16(const void* dy_bf16, const void* x_bf16, void* dw_bf16, int64_t rows, int64_t nf,
+                             int64_t kf, const int* padded_offsets, int groups, void* ws, size_t ws_bytes,
+                             void* stream) {
+    int rc = bwd_check("wgrad", dy_bf16, x_bf16, dw_bf16, rows, nf, kf, padded_offsets, groups, ws, ws_bytes, true);
+    if (rc) return rc;
+    nvfp4::GemmBf16Launch g{};
+    g.wgrad = 1;
+    g.dy = dy_bf16;
+    g.x = x_bf16;
+    g.out = dw_bf16;
+    g.rows = rows;
+    g.nf = (int)nf;
+    g.kf = (int)kf;
+    g.gpoff = padded_offsets;
+    g.G = padded_offsets ? groups : 1;
+    g.err = (ws != nullptr && ws_bytes >= 4) ? reinterpret_cast<uint32_t*>(ws) : nullptr;
+    g.num_sms = sm_count();
+    cudaError_t e = nvfp4::launch_gemm_bf16(g, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(NVFP4_ELAUNCH, "wgrad: %s", cudaGetErrorString(e));
     return ok();
 }
 

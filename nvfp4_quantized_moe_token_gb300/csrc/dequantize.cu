@@ -64,6 +64,7 @@ struct DequantArgs {
     const int* goff;   // nullable: scale rows padded per group (MoE buffers)
     const int* gpoff;
     int G;
+    int padded_rows;   // y rows at the padded positions too
     __nv_bfloat16* y;
     int64_t ldy;
 };
@@ -76,17 +77,20 @@ __global__ void __launch_bounds__(DQ_THREADS) dequantize_kernel(DequantArgs a) {
     const int nb = a.cols >> 4;
     if (r >= a.rows || b >= nb) return;
     int64_t srow = r;
+    int g = 0;
     if (a.goff != nullptr) {  // the group g with goff[g] <= r < goff[g + 1]
         int lo = 0, hi = a.G;
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
             if (__ldg(a.goff + mid) <= r) lo = mid; else hi = mid;
         }
+        g = lo;
         srow = (int64_t)__ldg(a.gpoff + lo) + (r - __ldg(a.goff + lo));
     }
     const int sp4 = (nb + 3) >> 2;
     const uint32_t sbyte = __ldg(a.sf + sf_group_offset(srow, b >> 2, sp4) + (b & 3));
-    const float sg = a.per_tensor ? __ldg(a.scale) : __ldg(a.scale + r);
+    // per-tensor with groups: one outer scale per group (the stacked expert weights)
+    const float sg = a.per_tensor ? __ldg(a.scale + g) : __ldg(a.scale + r);
     const uint2 cw = __ldg(reinterpret_cast<const uint2*>(a.codes + r * (a.cols >> 1)) + b);
     // s_b as f16x2 (both halves): q s_b has at most 6 significant bits and lies
     // in [2^-10, 2688], so the f16 product is exact
@@ -117,15 +121,32 @@ __global__ void __launch_bounds__(DQ_THREADS) dequantize_kernel(DequantArgs a) {
             w = bf16_of_product(v0, sg) | (bf16_of_product(v1, sg) << 16);
         o[i] = w;
     }
-    uint4* dst = reinterpret_cast<uint4*>(a.y + r * a.ldy + (int64_t)b * 16);
+    uint4* dst = reinterpret_cast<uint4*>(a.y + (a.padded_rows ? srow : r) * a.ldy + (int64_t)b * 16);
     dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
     dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// Zero the padding rows of the padded row layout: rows [gpoff[g] + (goff[g +
+// 1] - goff[g]), gpoff[g + 1]) of every group, 16 bytes per thread; the grid
+// covers a bound on gpoff[G] and threads past gpoff[G] return.
+__global__ void __launch_bounds__(DQ_THREADS) zero_padding_rows_kernel(DequantArgs a, int64_t chunks_per_row) {
+    const int64_t i = (int64_t)blockIdx.x * DQ_THREADS + threadIdx.x;
+    const int64_t pr = i / chunks_per_row;
+    const int64_t c = i - pr * chunks_per_row;
+    if (pr >= __ldg(a.gpoff + a.G)) return;
+    int lo = 0, hi = a.G;  // the group g with gpoff[g] <= pr < gpoff[g + 1]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(a.gpoff + mid) <= pr) lo = mid; else hi = mid;
+    }
+    if (pr - __ldg(a.gpoff + lo) < __ldg(a.goff + lo + 1) - __ldg(a.goff + lo)) return;  // a data row
+    reinterpret_cast<uint4*>(a.y + pr * a.ldy)[c] = make_uint4(0u, 0u, 0u, 0u);
 }
 
 }  // namespace
 
 cudaError_t launch_dequantize(const DequantLaunch& d, cudaStream_t stream) {
-    if (d.rows == 0) return cudaSuccess;
+    if (d.rows == 0 && !d.padded_rows) return cudaSuccess;
     DequantArgs a;
     a.codes = d.codes;
     a.sf = d.sf;
@@ -136,6 +157,7 @@ cudaError_t launch_dequantize(const DequantLaunch& d, cudaStream_t stream) {
     a.goff = d.goff;
     a.gpoff = d.gpoff;
     a.G = d.G;
+    a.padded_rows = d.padded_rows;
     a.y = reinterpret_cast<__nv_bfloat16*>(d.y);
     a.ldy = d.ldy;
     const int nb = a.cols / 16;
@@ -143,7 +165,15 @@ cudaError_t launch_dequantize(const DequantLaunch& d, cudaStream_t stream) {
     const int ty = DQ_THREADS / tx;                    // rows per CTA
     const int64_t gx = (a.rows + ty - 1) / ty;
     if (gx > 0x7FFFFFFF) return cudaErrorInvalidValue;
-    dequantize_kernel<<<dim3((unsigned)gx, (unsigned)((nb + tx - 1) / tx)), dim3(tx, ty), 0, stream>>>(a);
+    if (gx > 0) dequantize_kernel<<<dim3((unsigned)gx, (unsigned)((nb + tx - 1) / tx)), dim3(tx, ty), 0, stream>>>(a);
+    if (a.padded_rows) {
+        // padded rows number at most rows + 127 per group
+        const int64_t chunks = a.cols / 8;
+        const int64_t n = (a.rows + 127 * (int64_t)a.G) * chunks;
+        const int64_t blocks = (n + DQ_THREADS - 1) / DQ_THREADS;
+        if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
+        zero_padding_rows_kernel<<<(unsigned)blocks, DQ_THREADS, 0, stream>>>(a, chunks);
+    }
     return cudaGetLastError();
 }
 

@@ -31,12 +31,13 @@ cudaError_t launch_quantize(const QuantLaunch& q, cudaStream_t stream);
 struct DequantLaunch {
     const uint8_t* codes;   // [rows x cols/2]
     const uint8_t* sf;      // swizzled block scales
-    const float* scale;     // [rows], or [1] when per_tensor
+    const float* scale;     // [rows]; per_tensor: [1], or [G] (one per group) when goff is given
     int64_t rows, cols;
     int per_tensor;
     const int* goff;        // nullable: scale rows padded per group (goff/gpoff [G+1])
     const int* gpoff;
     int G;
+    int padded_rows;        // y rows follow the padded layout too (padding rows zeroed)
     void* y;                // bf16, row stride ldy elements
     int64_t ldy;
 };
@@ -70,6 +71,26 @@ struct GemmLaunch {
     int stall;             // test of the time-out path: the MMA thread waits on a barrier nothing arrives at
 };
 cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t stream);
+
+// Grouped BF16 GEMMs of the dequantized backward (tcgen05 kind::f16), over
+// row groups of the 128-row-padded expert layout (gpoff [G+1], multiples of
+// 128, padding rows zero) or one dense group of `rows` rows (gpoff null):
+//   dgrad (wgrad == 0): out [rows x kf] = dy [rows x nf] . w_g [nf x kf]
+//   wgrad (wgrad == 1): out_g [nf x kf] = dy[rows of g]^T . x[rows of g]
+struct GemmBf16Launch {
+    int wgrad;
+    const void* dy;        // bf16 [rows x nf]
+    const void* w;         // dgrad: bf16 [G*nf x kf] (w_g = DQ(Q(W_g)) as stored, [nf x kf])
+    const void* x;         // wgrad: bf16 [rows x kf]
+    void* out;             // dgrad: bf16 [rows x kf]; wgrad: bf16 [G*nf x kf]
+    int64_t rows;
+    int nf, kf;
+    const int* gpoff;      // nullable
+    int G;
+    uint32_t* err;         // nullable
+    int num_sms;
+};
+cudaError_t launch_gemm_bf16(const GemmBf16Launch& g, cudaStream_t stream);
 
 struct RouteLaunch {
     const float* logits;   // [T x E]

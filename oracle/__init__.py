@@ -378,6 +378,48 @@ def moe_forward(x_bf16, logits, bias, w1q, w2q, k, rows=None, w_deq=None, with_a
                 q2_codes=q2_codes, y2=y2, y2_abs=y2_abs, out=out)
 
 
+# ---------------------------------------------------------------- dequantized backward GEMMs
+
+def _groups(rows, poff):
+    if poff is None:
+        return [(0, rows)]
+    poff = np.asarray(poff, np.int64)
+    return [(int(poff[g]), int(poff[g + 1])) for g in range(len(poff) - 1)]
+
+
+def grouped_dgrad(dy_bf16, w_bf16, poff=None):
+    """dgrad of the dequantized backward ("Per-token NVFP4 and Dequantized
+    Backward", Improving Gradient Stability: BF16 backward on DQ(Q(w))): for
+    each row group g, dx[rows of g] = dy[rows of g] . w_g, in fp64 on the bf16
+    operands (each product exact).  dy bf16 bits [rows, nf], w bf16 bits
+    [G, nf, kf]; poff [G + 1] row offsets (None: one group).  Returns (dx fp64
+    [rows, kf], sum_n |dy w| per element)."""
+    dy = bf16_to_f64(dy_bf16)
+    w = bf16_to_f64(w_bf16)
+    dx = np.zeros((dy.shape[0], w.shape[2]))
+    ab = np.zeros_like(dx)
+    for g, (lo, hi) in enumerate(_groups(dy.shape[0], poff)):
+        dx[lo:hi] = dy[lo:hi] @ w[g]
+        ab[lo:hi] = np.abs(dy[lo:hi]) @ np.abs(w[g])
+    return dx, ab
+
+
+def grouped_wgrad(dy_bf16, x_bf16, poff=None, groups=None):
+    """wgrad of the dequantized backward: for each row group g, dw_g =
+    dy[rows of g]^T . x[rows of g] in fp64 on the bf16 operands (x = DQ(Q(x))).
+    dy bf16 bits [rows, nf], x bf16 bits [rows, kf].  Returns (dw fp64
+    [G, nf, kf], sum_r |dy x| per element); a group with no rows gives zero."""
+    dy = bf16_to_f64(dy_bf16)
+    x = bf16_to_f64(x_bf16)
+    gr = _groups(dy.shape[0], poff)
+    dw = np.zeros((len(gr), dy.shape[1], x.shape[1]))
+    ab = np.zeros_like(dw)
+    for g, (lo, hi) in enumerate(gr):
+        dw[g] = dy[lo:hi].T @ x[lo:hi]
+        ab[g] = np.abs(dy[lo:hi]).T @ np.abs(x[lo:hi])
+    return dw, ab
+
+
 # ---------------------------------------------------------------- single-pass FC2 (a research direction)
 
 def fc2_single_pass(d_bf16, w2q_e, k_tile=128):
