@@ -687,6 +687,67 @@ def weight_quantize_leg(local):
             "ms": ms, "gbs": nbytes / (ms / 1e3) / 1e9}
 
 
+def backward_leg(layer, local, reps=10):
+    """The dequantized BF16 backward of FC1 on the headline layer's own
+    operands: x^ = DQ(Q(x)) of the permuted quantized tokens written in the
+    128-row-padded layout, w^ = DQ(Q(W1)) of the 128 experts, a synthetic
+    gradient dY1 [Rp x 2F] (zero padding rows), then the grouped dgrad
+    (dX = dY1 . w^_e) and wgrad (dW1_e = dY1_e^T . x^_e), L2 flushed before
+    each launch.  Tensor-bound: FLOPs against the measured bf16 peak."""
+    nv = layer.nv
+    dev = torch.device("cuda", local)
+    peaks, src = load_peaks()
+    bf16_peak = peaks.get("bf16_tflops", 1900.0)
+    lay = nv.moe_workspace_layout(layer.T, H, F, E, K_TOP)
+    ws = layer.ws
+    R = layer.T * K_TOP
+    off = ws[lay["offsets"]:lay["offsets"] + 4 * (E + 1)].view(torch.int32)
+    poff = ws[lay["padded_offsets"]:lay["padded_offsets"] + 4 * (E + 1)].view(torch.int32)
+    Rp = int(poff[-1].item())
+    a1 = nv.NVFP4Tensor(ws[lay["a1_codes"]:lay["a1_codes"] + R * H // 2].view(R, H // 2),
+                        ws[lay["a1_sf"]:lay["a1_sf"] + Rp * H // 16],
+                        ws[lay["a1_scale"]:lay["a1_scale"] + 4 * R].view(torch.float32), R, H)
+    xh = torch.empty((Rp, H), dtype=torch.bfloat16, device=dev)
+    nv.dequantize_rows(a1, group_offsets=off, padded_offsets=poff, out=xh, padded_rows=True)
+    gw = torch.arange(0, (E + 1) * 2 * F, 2 * F, dtype=torch.int32, device=dev)
+    wh = nv.dequantize_rows(layer.w1q, per_tensor=True, group_offsets=gw, padded_offsets=gw).view(E, 2 * F, H)
+    # synthetic upstream gradient: data rows ~N(0, 1e-6), padding rows zero
+    pad = torch.ones(Rp, dtype=torch.bool, device=dev)
+    offs, poffs = off.long(), poff.long()
+    e_of = torch.repeat_interleave(torch.arange(E, device=dev), offs[1:] - offs[:-1])
+    prow = poffs[e_of] + (torch.arange(R, device=dev) - offs[e_of])
+    pad[prow] = False
+    dy = (torch.randn((Rp, 2 * F), device=dev) * 1e-3).to(torch.bfloat16)
+    dy[pad] = 0
+    dx = torch.empty((Rp, H), dtype=torch.bfloat16, device=dev)
+    dw = torch.empty((E, 2 * F, H), dtype=torch.bfloat16, device=dev)
+    err = torch.zeros(4, dtype=torch.int32, device=dev)
+    flush = L2Flush(dev)
+    for _ in range(2):
+        nv.grouped_dgrad_bf16(dy, wh, poff, out=dx, err=err)
+        nv.grouped_wgrad_bf16(dy, xh, poff, out=dw, err=err)
+    torch.cuda.synchronize()
+    if int(err[0].item()) != 0:
+        raise RuntimeError(f"backward GEMM error word {int(err[0].item()):#x}")
+    dg_ms = _timed(lambda: nv.grouped_dgrad_bf16(dy, wh, poff, out=dx, err=err), reps, flush)
+    wg_ms = _timed(lambda: nv.grouped_wgrad_bf16(dy, xh, poff, out=dw, err=err), reps, flush)
+    dq_ms = _timed(lambda: nv.dequantize_rows(a1, group_offsets=off, padded_offsets=poff, out=xh, padded_rows=True),
+                   reps, flush)
+    flop = 2.0 * Rp * (2 * F) * H  # both products: padded rows included (their MMAs run)
+    flop_valid = 2.0 * R * (2 * F) * H
+    out = {"workload": f"FC1 backward of the 32768-token layer: dX [Rp x {H}] = dY1 [Rp x {2 * F}] . w^_e; "
+                       f"dW1_e [{2 * F} x {H}] = dY1_e^T . x^_e; Rp = {Rp} padded rows ({R} token-expert rows)",
+           "dgrad_us": dg_ms * 1e3, "wgrad_us": wg_ms * 1e3, "dequant_x_padded_us": dq_ms * 1e3,
+           "dgrad_tflops": flop / (dg_ms / 1e3) / 1e12, "wgrad_tflops": flop / (wg_ms / 1e3) / 1e12,
+           "dgrad_frac": flop / (dg_ms / 1e3) / 1e12 / bf16_peak, "wgrad_frac": flop / (wg_ms / 1e3) / 1e12 / bf16_peak,
+           "valid_rows_tflops_dgrad": flop_valid / (dg_ms / 1e3) / 1e12,
+           "valid_rows_tflops_wgrad": flop_valid / (wg_ms / 1e3) / 1e12,
+           "peak_tflops": bf16_peak, "peak_source": f"{src} bf16 burst (cuBLAS)"}
+    del xh, wh, dy, dx, dw
+    torch.cuda.empty_cache()
+    return out
+
+
 def library_fp4_reference(local, reps=20):
     """The library NVFP4 GEMM (torch._scaled_mm on float4_e2m1fn_x2 operands
     with E4M3 16-element block scales, bf16 out) on dense problems of the
@@ -902,6 +963,9 @@ def summary_of(res):
         su = res["sustained"]
         out["sustained_tokens_per_s"] = su["tokens_per_s"]
         out["sustained_sm_mhz"] = (su.get("clocks") or {}).get("sm_mhz")
+    if res.get("backward_fc1_bf16"):
+        out["bwd_dgrad_frac_of_bf16"] = res["backward_fc1_bf16"]["dgrad_frac"]
+        out["bwd_wgrad_frac_of_bf16"] = res["backward_fc1_bf16"]["wgrad_frac"]
     if res.get("quant"):
         out["quant_us"] = res["quant"]["us"]
         out["quant_frac_of_hbm"] = res["quant"]["frac_of_hbm"]
@@ -930,6 +994,7 @@ def main():
     if rank == 0:
         if not args.quick:
             res["sustained"] = sustained_leg(layer, local)
+            res["backward_fc1_bf16"] = backward_leg(layer, local)
             del layer
             torch.cuda.empty_cache()
             res["moe_8k"] = moe_8k_leg(nv, local, args.steps, args.warmup)

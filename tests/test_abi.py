@@ -46,6 +46,8 @@ def test_binding_structs_and_error_bits_match_the_header():
     assert _struct_fields(src, "nvfp4_tensor") == [f[0] for f in nv._Tensor._fields_]
     bits = dict(re.findall(r"#define NVFP4_DEVERR_(\w+) (\d+)u", src))
     assert int(bits["TIMEOUT"]) == nv.DEVERR_TIMEOUT and int(bits["BADEXPERT"]) == nv.DEVERR_BADEXPERT
+    assert int(bits["BADGROUP"]) == nv.DEVERR_BADGROUP
+    assert int(re.search(r"#define NVFP4_DQ_PADDED_ROWS (\d+)", src).group(1)) == nv.DQ_PADDED_ROWS
 
 
 def test_every_declared_symbol_is_exported(L):
@@ -138,3 +140,27 @@ def test_quantize_grouped_rejects_bad_arguments(L):
     assert call(wsb=16 + 4 * 4 - 1) == -4
     assert call(ws=None) == -4
     assert L.nvfp4_last_error().decode()
+
+
+def test_backward_gemms_reject_bad_arguments(L):
+    """Host-side checks of the grouped BF16 backward GEMMs (no device work happens)."""
+    for fn, nf_mult in ((L.nvfp4_grouped_dgrad_bf16, 64), (L.nvfp4_grouped_wgrad_bf16, 256)):
+        def call(a=4096, b=4096, c=4096, rows=256, nf=512, kf=512, poff=None, groups=1, ws=None, wsb=0):
+            return fn(a, b, c, rows, nf, kf, poff, groups, ws, wsb, None)
+        assert call(a=None) == -1
+        assert call(c=None) == -1
+        assert call(rows=-1) == -2
+        assert call(kf=320) == -2                 # output columns: multiples of 256
+        assert call(nf=nf_mult + 32) == -2        # dgrad contraction / wgrad output rows
+        assert call(poff=4096, groups=0) == -2
+        assert call(poff=4096, groups=257) == -2
+        assert call(a=4096 + 8) == -3
+        assert call(ws=4098, wsb=64) == -3
+        assert L.nvfp4_last_error().decode()
+
+
+def test_dequantize_padded_rows_needs_offsets(L):
+    t = _t(64, 256)
+    assert L.nvfp4_dequantize_rows(ctypes.byref(t), nv.PER_ROW | nv.DQ_PADDED_ROWS, None, None, 0, 4096, 256,
+                                   None) == -1
+    assert L.nvfp4_dequantize_rows(ctypes.byref(t), 64, None, None, 0, 4096, 256, None) == -1
