@@ -291,3 +291,14 @@ def test_bf16_ulp_is_the_gap_to_the_next_bf16_value():
     # the smallest subnormal spacing holds from zero through the top of the subnormal range
     assert oracle.bf16_ulp(0.0) == 2.0 ** -133 and oracle.bf16_ulp(2.0 ** -126) == 2.0 ** -133
     assert oracle.bf16_ulp(1.0) == 2.0 ** -7 and oracle.bf16_ulp(np.nextafter(2.0, 0.0)) == 2.0 ** -7
+
+
+def test_error_metrics_closed_forms():
+    """rel-L2, SNR (dB) and MAE of a reconstruction ("miniTE Technical Report"
+    2.3) on vectors whose values are known in closed form."""
+    x = np.array([3.0, 4.0, 0.0, 0.0])
+    m = oracle.error_metrics(x, x + np.array([0.0, 0.0, 0.5, -0.5]))
+    assert np.isclose(m["rel_l2"], np.sqrt(0.5) / 5.0)
+    assert np.isclose(m["snr_db"], 20 * np.log10(5.0 / np.sqrt(0.5)))
+    assert np.isclose(m["mae"], 0.25)
+    assert oracle.error_metrics(x, x)["snr_db"] == np.inf
