@@ -75,8 +75,9 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--quick", action="store_true", help="profiling runs: no e2e, no oracle, no clocks")
-    p.add_argument("--only", choices=["all", "quant", "dequant"], default="all",
-                   help="quant / dequant: time only the 16384 x 2048 quantizer / dequantizer workload (for profiling)")
+    p.add_argument("--only", choices=["all", "quant", "dequant", "backward"], default="all",
+                   help="quant / dequant: time only the 16384 x 2048 quantizer / dequantizer workload; backward: "
+                        "only the FC1 backward GEMMs of the 32768-token layer (for profiling)")
     return p.parse_args()
 
 
@@ -985,6 +986,13 @@ def main():
         return
     import nvfp4_quantized_moe_token_gb300 as nv
     nv.lib()
+    if args.only == "backward":
+        if rank == 0:
+            layer = Layer(nv, torch.device("cuda", local), make_inputs())
+            layer()
+            torch.cuda.synchronize()
+            print(json.dumps({"backward_fc1_bf16": backward_leg(layer, local, reps=max(args.steps, 1))}))
+        return
     if args.only in ("quant", "dequant"):
         if rank == 0:
             fn = quant_gbs if args.only == "quant" else dequant_gbs

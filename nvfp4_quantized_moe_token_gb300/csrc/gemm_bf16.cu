@@ -76,6 +76,7 @@ struct __align__(1024) Smem {
     int bad;                     // group offsets not multiples of 128 or not ascending: nothing is computed
     int gpoff[MAX_G + 1];
     int ppre[MAX_G + 1];         // dgrad: units of m-tile pairs before each group
+    int order[MAX_G];            // wgrad: groups by decreasing row count (ties: lower index first)
 };
 static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory per CTA");
 static_assert(offsetof(Smem, stg) % 1024 == 0, "staging alignment (128B swizzle atoms)");
@@ -156,8 +157,9 @@ __device__ __forceinline__ Unit decode_unit(const Smem& s, const Params& p, int 
     } else {
         const int m_pairs = p.Mo / (2 * BM);
         const int per_g = m_pairs * n_tiles;
-        x.g = u / per_g;
-        const int r = u - x.g * per_g;
+        const int gi = u / per_g;
+        x.g = s.order[gi];
+        const int r = u - gi * per_g;
         const int mp = r / n_tiles;
         x.n0 = (r - mp * n_tiles) * TN;
         x.m0 = mp * 2 * BM + (int)rank * BM;
@@ -212,6 +214,22 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     if (warp == 0 && lane == 0) { prefetch_tmap(&tmA); prefetch_tmap(&tmB); prefetch_tmap(&tmO); }
     if (warp == 1) { tmem_alloc2(smem_u32(&s.tmem_base), TMEM_COLS); tmem_relinquish2(); }
     __syncthreads();
+    if (WGRAD) {
+        // Largest groups first: a unit's cost is its group's row count, and the
+        // pairs take units in a fixed stride, so the long units start first and
+        // the short ones fill the end (the skewed routing of the expert layer
+        // leaves a few groups several times the mean).  Rank of g = groups with
+        // more rows, or as many rows and a lower index.
+        for (int g = threadIdx.x; g < G; g += THREADS) {
+            const int n = s.gpoff[g + 1] - s.gpoff[g];
+            int rank_g = 0;
+            for (int h = 0; h < G; ++h) {
+                const int m = s.gpoff[h + 1] - s.gpoff[h];
+                rank_g += (m > n) || (m == n && h < g);
+            }
+            s.order[rank_g] = g;
+        }
+    }
     if (!WGRAD && warp == 0) {
         // ppre[g] = pair rows before group g; lane l holds groups 8l .. 8l + 7
         int loc[8], sum = 0;
