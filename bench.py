@@ -995,8 +995,12 @@ def main():
         return
     if args.only in ("quant", "dequant"):
         if rank == 0:
-            fn = quant_gbs if args.only == "quant" else dequant_gbs
-            print(json.dumps({args.only: fn(args, local, reps=max(args.steps, 1))}))
+            if args.only == "quant":
+                out = {"quant": quant_gbs(args, local, reps=max(args.steps, 1)),
+                       "quant_four_over_six": quant_gbs(args, local, reps=max(args.steps, 1), four_over_six="mse")}
+            else:
+                out = {"dequant": dequant_gbs(args, local, reps=max(args.steps, 1))}
+            print(json.dumps(out))
         return
     res, d, layer = run_ours(args, rank, world, local)
     if rank == 0:

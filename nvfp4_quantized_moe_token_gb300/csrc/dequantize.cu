@@ -75,18 +75,27 @@ __global__ void __launch_bounds__(DQ_THREADS) dequantize_kernel(DequantArgs a) {
     const int64_t r = (int64_t)blockIdx.x * blockDim.y + threadIdx.y;
     const int b = (int)(blockIdx.y * blockDim.x + threadIdx.x);
     const int nb = a.cols >> 4;
-    if (r >= a.rows || b >= nb) return;
     int64_t srow = r;
     int g = 0;
-    if (a.goff != nullptr) {  // the group g with goff[g] <= r < goff[g + 1]
-        int lo = 0, hi = a.G;
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (__ldg(a.goff + mid) <= r) lo = mid; else hi = mid;
+    if (a.goff != nullptr) {
+        // the group g with goff[g] <= r < goff[g + 1]: a warp's lanes share one row
+        // whenever a row spans whole warps (blockDim.x a multiple of 32), so one lane
+        // searches and the others take its answer; otherwise every lane searches
+        const bool shared_row = (blockDim.x & 31) == 0;
+        const int lane = threadIdx.x & 31;
+        if (!shared_row || lane == 0) {
+            int lo = 0, hi = a.G;
+            const int64_t rr = r < a.rows ? r : a.rows - 1;
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (__ldg(a.goff + mid) <= rr) lo = mid; else hi = mid;
+            }
+            g = lo;
         }
-        g = lo;
-        srow = (int64_t)__ldg(a.gpoff + lo) + (r - __ldg(a.goff + lo));
+        if (shared_row) g = __shfl_sync(0xffffffffu, g, 0);
+        srow = (int64_t)__ldg(a.gpoff + g) + (r - __ldg(a.goff + g));
     }
+    if (r >= a.rows || b >= nb) return;
     const int sp4 = (nb + 3) >> 2;
     const uint32_t sbyte = __ldg(a.sf + sf_group_offset(srow, b >> 2, sp4) + (b & 3));
     // per-tensor with groups: one outer scale per group (the stacked expert weights)
@@ -127,19 +136,16 @@ __global__ void __launch_bounds__(DQ_THREADS) dequantize_kernel(DequantArgs a) {
 }
 
 // Zero the padding rows of the padded row layout: rows [gpoff[g] + (goff[g +
-// 1] - goff[g]), gpoff[g + 1]) of every group, 16 bytes per thread; the grid
-// covers a bound on gpoff[G] and threads past gpoff[G] return.
-__global__ void __launch_bounds__(DQ_THREADS) zero_padding_rows_kernel(DequantArgs a, int64_t chunks_per_row) {
+// 1] - goff[g]), gpoff[g + 1]) of group g = blockIdx.y (at most 127 rows),
+// 16 bytes per thread.
+__global__ void __launch_bounds__(DQ_THREADS) zero_padding_rows_kernel(DequantArgs a, int chunks_per_row) {
+    const int g = blockIdx.y;
+    const int64_t start = (int64_t)__ldg(a.gpoff + g) + (__ldg(a.goff + g + 1) - __ldg(a.goff + g));
+    const int64_t end = __ldg(a.gpoff + g + 1);
     const int64_t i = (int64_t)blockIdx.x * DQ_THREADS + threadIdx.x;
-    const int64_t pr = i / chunks_per_row;
-    const int64_t c = i - pr * chunks_per_row;
-    if (pr >= __ldg(a.gpoff + a.G)) return;
-    int lo = 0, hi = a.G;  // the group g with gpoff[g] <= pr < gpoff[g + 1]
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (__ldg(a.gpoff + mid) <= pr) lo = mid; else hi = mid;
-    }
-    if (pr - __ldg(a.gpoff + lo) < __ldg(a.goff + lo + 1) - __ldg(a.goff + lo)) return;  // a data row
+    const int64_t pr = start + i / chunks_per_row;
+    if (pr >= end) return;
+    const int64_t c = i % chunks_per_row;
     reinterpret_cast<uint4*>(a.y + pr * a.ldy)[c] = make_uint4(0u, 0u, 0u, 0u);
 }
 
@@ -167,12 +173,10 @@ cudaError_t launch_dequantize(const DequantLaunch& d, cudaStream_t stream) {
     if (gx > 0x7FFFFFFF) return cudaErrorInvalidValue;
     if (gx > 0) dequantize_kernel<<<dim3((unsigned)gx, (unsigned)((nb + tx - 1) / tx)), dim3(tx, ty), 0, stream>>>(a);
     if (a.padded_rows) {
-        // padded rows number at most rows + 127 per group
-        const int64_t chunks = a.cols / 8;
-        const int64_t n = (a.rows + 127 * (int64_t)a.G) * chunks;
-        const int64_t blocks = (n + DQ_THREADS - 1) / DQ_THREADS;
-        if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
-        zero_padding_rows_kernel<<<(unsigned)blocks, DQ_THREADS, 0, stream>>>(a, chunks);
+        // each group pads at most 127 rows
+        const int chunks = a.cols / 8;
+        const unsigned bx = (unsigned)((127 * (int64_t)chunks + DQ_THREADS - 1) / DQ_THREADS);
+        zero_padding_rows_kernel<<<dim3(bx, (unsigned)a.G), DQ_THREADS, 0, stream>>>(a, chunks);
     }
     return cudaGetLastError();
 }
