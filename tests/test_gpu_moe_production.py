@@ -93,3 +93,43 @@ def test_end_to_end_against_the_oracle_chain(name, n_tok):
           f"q2 code mismatch rate {mism:.3e} ({rows_flipped:.3%} of {len(rows)} rows with a flip)")
     assert rel <= 1e-3, rel
     assert within >= 0.999, within
+
+
+def test_graph_replay_is_bit_identical_to_the_eager_call():
+    """The layer captured once into a CUDA graph and replayed (how bench.py
+    times the step, and how a serving loop of fixed shape would run it): same
+    bits as the eager call, on two replays with different inputs copied into
+    the captured buffers in between."""
+    rng = np.random.default_rng(21)
+    T, E_, k, H, F_ = 700, 64, 8, 512, 256
+    w1q = nv.quantize_grouped_weights(to_dev_bf16(workloads.gaussian_bf16(rng, (E_, 2 * F_, H), std=0.02)))
+    w2q = nv.quantize_grouped_weights(to_dev_bf16(workloads.gaussian_bf16(rng, (E_, H, F_), std=0.02)))
+    x = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    lg = torch.empty((T, E_), dtype=torch.float32, device="cuda")
+    bs = torch.empty((E_,), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(int(nv.lib().moe_expert_workspace(T, H, F_, E_, k)), dtype=torch.uint8, device="cuda")
+    out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+
+    def fill(seed):
+        r = np.random.default_rng(seed)
+        x.copy_(to_dev_bf16(workloads.gaussian_bf16(r, (T, H))))
+        lg.copy_(torch.from_numpy(r.standard_normal((T, E_), dtype=np.float32)))
+        bs.copy_(torch.from_numpy(r.standard_normal(E_, dtype=np.float32)))
+
+    fill(1)
+    nv.moe_expert_forward(x, lg, bs, w1q, w2q, F_, k, out=out, ws=ws)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        nv.moe_expert_forward(x, lg, bs, w1q, w2q, F_, k, out=out, ws=ws)
+    torch.cuda.current_stream().wait_stream(side)
+    for seed in (2, 3):
+        fill(seed)
+        g.replay()
+        torch.cuda.synchronize()
+        got = out.clone()
+        ref, _ = nv.moe_expert_forward(x, lg, bs, w1q, w2q, F_, k)
+        torch.cuda.synchronize()
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16)), f"replay with inputs {seed}"
