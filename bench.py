@@ -808,6 +808,34 @@ def backward_leg(layer, local, reps=10):
                    reps, flush)
     flop = 2.0 * Rp * (2 * F) * H  # both products: padded rows included (their MMAs run)
     flop_valid = 2.0 * R * (2 * F) * H
+    del xh, wh, dx, dw
+    # FC2's backward on its own operands: d^ = DQ(Q(D)) of the requantized SwiGLU output (a2) in
+    # the padded layout, w2^ = DQ(Q(W2)) per expert, a synthetic dY2 [Rp x H]
+    a2 = nv.NVFP4Tensor(ws[lay["a2_codes"]:lay["a2_codes"] + R * F // 2].view(R, F // 2),
+                        ws[lay["a2_sf"]:lay["a2_sf"] + Rp * ((F // 16 + 3) // 4 * 4)],
+                        ws[lay["a2_scale"]:lay["a2_scale"] + 4 * R].view(torch.float32), R, F)
+    dh = torch.empty((Rp, F), dtype=torch.bfloat16, device=dev)
+    nv.dequantize_rows(a2, group_offsets=off, padded_offsets=poff, out=dh, padded_rows=True)
+    gw2 = torch.arange(0, (E + 1) * H, H, dtype=torch.int32, device=dev)
+    wh2 = nv.dequantize_rows(layer.w2q, per_tensor=True, group_offsets=gw2, padded_offsets=gw2).view(E, H, F)
+    dy2 = (torch.randn((Rp, H), device=dev) * 1e-3).to(torch.bfloat16)
+    dy2[pad] = 0
+    dd = torch.empty((Rp, F), dtype=torch.bfloat16, device=dev)
+    dw2 = torch.empty((E, H, F), dtype=torch.bfloat16, device=dev)
+    nv.grouped_dgrad_bf16(dy2, wh2, poff, out=dd, err=err)
+    nv.grouped_wgrad_bf16(dy2, dh, poff, out=dw2, err=err)
+    torch.cuda.synchronize()
+    if int(err[0].item()) != 0:
+        raise RuntimeError(f"backward GEMM error word {int(err[0].item()):#x}")
+    dg2_ms = _timed(lambda: nv.grouped_dgrad_bf16(dy2, wh2, poff, out=dd, err=err), reps, flush)
+    wg2_ms = _timed(lambda: nv.grouped_wgrad_bf16(dy2, dh, poff, out=dw2, err=err), reps, flush)
+    flop2 = 2.0 * Rp * H * F
+    fc2 = {"workload": f"FC2 backward: dD [Rp x {F}] = dY2 [Rp x {H}] . w2^_e; dW2_e [{H} x {F}] = dY2_e^T . d^_e",
+           "dgrad_us": dg2_ms * 1e3, "wgrad_us": wg2_ms * 1e3,
+           "dgrad_tflops": flop2 / (dg2_ms / 1e3) / 1e12, "wgrad_tflops": flop2 / (wg2_ms / 1e3) / 1e12,
+           "dgrad_frac": flop2 / (dg2_ms / 1e3) / 1e12 / bf16_peak,
+           "wgrad_frac": flop2 / (wg2_ms / 1e3) / 1e12 / bf16_peak}
+    del dh, wh2, dy2, dd, dw2
     out = {"workload": f"FC1 backward of the 32768-token layer: dX [Rp x {H}] = dY1 [Rp x {2 * F}] . w^_e; "
                        f"dW1_e [{2 * F} x {H}] = dY1_e^T . x^_e; Rp = {Rp} padded rows ({R} token-expert rows)",
            "dgrad_us": dg_ms * 1e3, "wgrad_us": wg_ms * 1e3, "dequant_x_padded_us": dq_ms * 1e3,
@@ -815,8 +843,8 @@ def backward_leg(layer, local, reps=10):
            "dgrad_frac": flop / (dg_ms / 1e3) / 1e12 / bf16_peak, "wgrad_frac": flop / (wg_ms / 1e3) / 1e12 / bf16_peak,
            "valid_rows_tflops_dgrad": flop_valid / (dg_ms / 1e3) / 1e12,
            "valid_rows_tflops_wgrad": flop_valid / (wg_ms / 1e3) / 1e12,
-           "peak_tflops": bf16_peak, "peak_source": f"{src} bf16 burst (cuBLAS)"}
-    del xh, wh, dy, dx, dw
+           "peak_tflops": bf16_peak, "peak_source": f"{src} bf16 burst (cuBLAS)", "fc2": fc2}
+    del dy
     torch.cuda.empty_cache()
     return out
 
