@@ -75,6 +75,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--quick", action="store_true", help="profiling runs: no e2e, no oracle, no clocks")
+    p.add_argument("--tokens", type=int, choices=[8192, 32768], default=32768,
+                   help="--only backward: the layer whose backward is timed (8192: a smaller case for profiling)")
     p.add_argument("--only", choices=["all", "quant", "dequant", "backward"], default="all",
                    help="quant / dequant: time only the 16384 x 2048 quantizer / dequantizer workload; backward: "
                         "only the FC1 backward GEMMs of the 32768-token layer (for profiling)")
@@ -1090,7 +1092,8 @@ def main():
     nv.lib()
     if args.only == "backward":
         if rank == 0:
-            layer = Layer(nv, torch.device("cuda", local), make_inputs())
+            d = make_inputs() if args.tokens == 32768 else workloads.moe_8k()
+            layer = Layer(nv, torch.device("cuda", local), d)
             layer()
             torch.cuda.synchronize()
             print(json.dumps({"backward_fc1_bf16": backward_leg(layer, local, reps=max(args.steps, 1))}))
