@@ -263,7 +263,26 @@ typedef struct moe_options {
      * block scaling of the activations (X and the FC2 input D).  Weights
      * take it through their own nvfp4_quantize_rows call. */
     int four_over_six;
+    /* Where the FC2 input D is requantized ("miniTE Technical Report" 5.6:
+     * moving the quantization into the consumer GEMM so that the quantized
+     * copy is never written).
+     *   MOE_REQUANT_AUTO (0): the library's choice: MOE_REQUANT_SEPARATE.
+     *   MOE_REQUANT_SEPARATE (1): a quantization launch between FC1 and FC2
+     *     reads D back and writes its codes, block scales and row scales to
+     *     the workspace; FC2 loads them.
+     *   MOE_REQUANT_IN_FC2 (2): FC2 reads D and FC1's row amax and encodes
+     *     each 128-row tile of A in shared memory (the same codes and scales,
+     *     bit for bit), reusing it for all of the tile's output columns.  Only
+     *     for plain NVFP4 activations (four_over_six 0), F a multiple of 256
+     *     up to 768 and H of at least 512; other layers take the separate
+     *     launch.  The workspace's requantized copies (a2_codes, a2_sf,
+     *     a2_scale) are then written only on request (moe_debug.requant_copy). */
+    int fc2_requant;
 } moe_options;
+
+#define MOE_REQUANT_AUTO 0
+#define MOE_REQUANT_SEPARATE 1
+#define MOE_REQUANT_IN_FC2 2
 
 /* Optional debug outputs of moe_expert_forward (all nullable, device).
  * Zero-initialise the whole struct (moe_debug d = {0};) and set only the
@@ -276,7 +295,9 @@ typedef struct moe_debug {
      * entry is skipped) recorded on `stream` before the first stage and after
      * each stage: quantize X
      * (with the router top-k, launched together), routing metadata +
-     * permute, FC1, requant, FC2, combine. */
+     * permute, FC1, requant, FC2, combine.  With the requantization inside
+     * FC2 the requant stage is empty (its two events are recorded back to
+     * back) and the FC2 stage holds both. */
     void** stage_events;
     /* Nonzero: FC1's MMA-issuing thread first waits on a barrier that
      * nothing arrives at, so that its bounded wait runs out (a test of the
@@ -285,6 +306,11 @@ typedef struct moe_debug {
      * and returns; the layer's outputs are undefined, the context stays
      * usable.  Takes about 2 s.  0 for normal operation. */
     int stall_fc1;
+    /* Nonzero: with the requantization inside FC2 (moe_options.fc2_requant),
+     * FC2 also writes the codes, block scales and row scales it encodes to
+     * the workspace's a2_codes / a2_sf / a2_scale, where the separate launch
+     * leaves them.  0: they are not written. */
+    int requant_copy;
 } moe_debug;
 
 #define MOE_STAGE_EVENTS 7

@@ -25,11 +25,12 @@ class _Tensor(ctypes.Structure):
 
 
 class _Options(ctypes.Structure):
-    _fields_ = [("weight_at_fc1", ctypes.c_int), ("four_over_six", ctypes.c_int)]
+    _fields_ = [("weight_at_fc1", ctypes.c_int), ("four_over_six", ctypes.c_int), ("fc2_requant", ctypes.c_int)]
 
 
 class _Debug(ctypes.Structure):
-    _fields_ = [("fc1_out", c_vp), ("stage_events", ctypes.POINTER(c_vp)), ("stall_fc1", ctypes.c_int)]
+    _fields_ = [("fc1_out", c_vp), ("stage_events", ctypes.POINTER(c_vp)), ("stall_fc1", ctypes.c_int),
+                ("requant_copy", ctypes.c_int)]
 
 
 STAGES = ["quantize", "route", "fc1", "requant", "fc2", "combine"]
@@ -51,6 +52,7 @@ DEVERR_TIMEOUT = 1    # bits of the device error word
 DEVERR_BADEXPERT = 2
 DEVERR_BADGROUP = 4
 FOUR_OVER_SIX = {None: 0, "mse": 2, "mae": 4}  # scale-mode flags of four-over-six block scaling
+FC2_REQUANT = {None: 0, "separate": 1, "in_fc2": 2}  # moe_options.fc2_requant
 SYMBOLS = ["nvfp4_sf_bytes", "nvfp4_quantize_workspace", "nvfp4_quantize_rows", "nvfp4_quantize_grouped",
            "nvfp4_dequantize_rows",
            "nvfp4_linear", "nvfp4_grouped_dgrad_bf16", "nvfp4_grouped_wgrad_bf16",
@@ -255,9 +257,12 @@ def moe_workspace_layout(T, H, F, E, topk):
 
 def moe_expert_forward(x, logits, bias, w1q, w2q, F, topk, weight_at_fc1=False, out=None,
                        ws=None, fc1_debug=None, stage_events=None, four_over_six=None, stream=None,
-                       debug_stall_fc1=False):
+                       debug_stall_fc1=False, fc2_requant=None, requant_copy=False):
     """One W4A4 MoE expert layer on the device.  Returns (out bf16 [T, H], ws).
     four_over_six (None, 'mse', 'mae'): four-over-six scaling of the activations.
+    fc2_requant (None: the library's choice, 'separate', 'in_fc2'): where D is
+    requantized (moe_options.fc2_requant); requant_copy: with 'in_fc2', also
+    write the encoded D to the workspace's a2 slots (moe_debug.requant_copy).
     debug_stall_fc1: test of the time-out path (moe_debug.stall_fc1): FC1's
     bounded wait runs out, DEVERR_TIMEOUT is set in the workspace's error
     word, the outputs are undefined.
@@ -273,7 +278,7 @@ def moe_expert_forward(x, logits, bias, w1q, w2q, F, topk, weight_at_fc1=False, 
     if out is None:
         out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
     a, b = w1q.c(), w2q.c()
-    opt = _Options(1 if weight_at_fc1 else 0, FOUR_OVER_SIX[four_over_six])
+    opt = _Options(1 if weight_at_fc1 else 0, FOUR_OVER_SIX[four_over_six], FC2_REQUANT[fc2_requant])
     evs = None
     if stage_events is not None:
         assert len(stage_events) == len(STAGES) + 1
@@ -282,7 +287,8 @@ def moe_expert_forward(x, logits, bias, w1q, w2q, F, topk, weight_at_fc1=False, 
             if e is not None and e.cuda_event == 0:  # torch creates the CUDA event on its first record
                 e.record(st)
         evs = (c_vp * len(stage_events))(*[None if e is None else e.cuda_event for e in stage_events])
-    dbg = _Debug(None if fc1_debug is None else fc1_debug.data_ptr(), evs, 1 if debug_stall_fc1 else 0)
+    dbg = _Debug(None if fc1_debug is None else fc1_debug.data_ptr(), evs, 1 if debug_stall_fc1 else 0,
+                 1 if requant_copy else 0)
     rc = lib().moe_expert_forward(_ptr(x), T, H, _ptr(logits), _ptr(bias), E, topk, ctypes.byref(a),
                                   ctypes.byref(b), F, ctypes.byref(opt), _ptr(out), ctypes.byref(dbg),
                                   _ptr(ws), ws.numel(), _stream(stream))

@@ -14,7 +14,7 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libnvfp4moe.so")
 SOURCES = ["api.cu", "quantize.cu", "dequantize.cu", "route.cu", "gemm.cu", "gemm_bf16.cu", "combine.cu",
            "noalloc.cu"]
-HEADERS = ["common.cuh", "fastdiv.cuh", "route_topk.cuh", "kernels.h", os.path.join("..", "..", "include", "nvfp4moe.h")]
+HEADERS = ["common.cuh", "fastdiv.cuh", "nvfp4_encode.cuh", "route_topk.cuh", "kernels.h", os.path.join("..", "..", "include", "nvfp4moe.h")]
 
 NVCC = os.environ.get("NVCC", shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc")
 FLAGS = [

@@ -388,6 +388,9 @@ int moe_expert_forward(const void* x_bf16, int64_t T, int64_t H, const float* ro
     if (!fos_flags_valid(fos_flags) || (fos_flags != 0 && fos_flags != NVFP4_FOUR_OVER_SIX_MSE &&
                                         fos_flags != NVFP4_FOUR_OVER_SIX_MAE))
         return fail(NVFP4_EINVAL, "moe: four_over_six must be 0, NVFP4_FOUR_OVER_SIX_MSE or _MAE");
+    const int requant = opt != nullptr ? opt->fc2_requant : MOE_REQUANT_AUTO;
+    if (requant < MOE_REQUANT_AUTO || requant > MOE_REQUANT_IN_FC2)
+        return fail(NVFP4_EINVAL, "moe: fc2_requant must be MOE_REQUANT_AUTO, _SEPARATE or _IN_FC2");
     if (sm_count() <= 0) return fail(NVFP4_ELAUNCH, "moe: no CUDA device");
     const bool at_fc1 = opt != nullptr && opt->weight_at_fc1 != 0;
     const int fos = fos_of(fos_flags);
@@ -481,7 +484,9 @@ int moe_expert_forward(const void* x_bf16, int64_t T, int64_t H, const float* ro
     if ((e = nvfp4::launch_gemm(g1, s)) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe fc1: %s", cudaGetErrorString(e));
     if ((e = mark()) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe event: %s", cudaGetErrorString(e));
 
-    // 4. requantize D per row, reusing the epilogue's amax
+    // 4. requantize D per row, reusing the epilogue's amax: a separate launch,
+    //    or inside FC2 (plain NVFP4, F a multiple of 256 up to 768, H >= 512)
+    const bool in_fc2 = requant == MOE_REQUANT_IN_FC2 && fos == 0 && F % 256 == 0 && F <= 768 && H >= 512;
     nvfp4::QuantLaunch q2{};
     q2.x = at(L.d);
     q2.ld = F;
@@ -497,7 +502,8 @@ int moe_expert_forward(const void* x_bf16, int64_t T, int64_t H, const float* ro
     q2.reverse = 1;  // FC1's last rows are still in L2; FC2 then starts on the rows written last
     q2.fos = fos;
     q2.err = reinterpret_cast<uint32_t*>(at(L.err));
-    if ((e = nvfp4::launch_quantize(q2, s)) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe requant: %s", cudaGetErrorString(e));
+    if (!in_fc2 && (e = nvfp4::launch_quantize(q2, s)) != cudaSuccess)
+        return fail(NVFP4_ELAUNCH, "moe requant: %s", cudaGetErrorString(e));
     if ((e = mark()) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe event: %s", cudaGetErrorString(e));
 
     // 5. FC2 grouped GEMM -> bf16 Y2
@@ -514,7 +520,16 @@ int moe_expert_forward(const void* x_bf16, int64_t T, int64_t H, const float* ro
     g2.G = E;
     g2.goff = r.off;
     g2.gpoff = r.poff;
-    g2.mode = 0;
+    g2.mode = in_fc2 ? 3 : 0;
+    if (in_fc2) {
+        g2.d_in = at(L.d);
+        g2.d_amax = reinterpret_cast<const float*>(at(L.amax2));
+        if (dbg != nullptr && dbg->requant_copy) {  // copies of the encoded A, where the separate launch writes them
+            g2.q_codes = at(L.a2_codes);
+            g2.q_sf = at(L.a2_sf);
+            g2.q_scale = reinterpret_cast<float*>(at(L.a2_scale));
+        }
+    }
     g2.out = at(L.y2);
     g2.ldo = H;
     g2.err = r.err;

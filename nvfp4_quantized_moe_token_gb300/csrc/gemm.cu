@@ -62,6 +62,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "nvfp4_encode.cuh"
 
 namespace nvfp4 {
 
@@ -95,6 +96,12 @@ constexpr int MAX_G = 256;
 // Mode 2 is the plain epilogue for long K loops (K >= 1024, the dense
 // linear): 5 stages in flight, and each warp's 64 columns leave as two
 // 32-column boxes through one staging box (the smem of a fifth stage).
+// Mode 3 is mode 0 with its A operand quantized in the kernel (FC2 of the
+// expert layer, K <= 768): the epilogue warps read the bf16 rows of D and
+// the row amax that FC1's epilogue left, encode them into a resident A tile
+// (codes in the MMA's swizzled layout, block scales as atoms) and the row
+// scales; a pair then runs all n-tiles of its m-tiles back to back on that
+// tile.  B streams through the 4-stage ring as in mode 0.
 template <int MODE>
 struct Cfg {
     static constexpr int BK = 256;                      // FP4 elements of K per stage
@@ -103,8 +110,11 @@ struct Cfg {
     static constexpr int ACC_BUFS = 1;                  // accumulators in TMEM (2 fit at TN = 128)
     static constexpr int B_ROWS = TN / 2;               // weight rows staged per CTA (half the tile)
     static constexpr int SFB_BLOCKS = TN / 128;         // 128-row weight-scale blocks per tile
-    static constexpr bool PLAIN = MODE != 1;            // modes 0 and 2: plain bf16 out
-    static constexpr int STAGES = MODE == 0 ? 4 : 5;
+    static constexpr bool PLAIN = MODE != 1;            // modes 0, 2 and 3: plain bf16 out
+    static constexpr bool QOL = MODE == 3;              // A quantized on load, resident across n-tiles
+    static constexpr int STAGES = (MODE == 0 || MODE == 3) ? 4 : 5;
+    static constexpr int KCH = 3;                       // mode 3: K-stages of the resident A tile (K <= 768)
+    static constexpr int A_SLOTS = QOL ? KCH : STAGES;  // A slots: the ring, or the resident tile's stages
     static constexpr int NBUF = 1;                      // staging boxes per epilogue warp
     static constexpr int A_BYTES = BM * ROWB;           // this CTA's 128 rows of A
     static constexpr int B_BYTES = B_ROWS * ROWB;       // this CTA's half of the weight rows
@@ -116,7 +126,7 @@ struct Cfg {
     static constexpr uint32_t SF_STAGE_COLS = 4 * ATOMS * (1 + SFB_BLOCKS);  // SFA 4 + SFB 4 per block, per atom
     static constexpr uint32_t IDESC = idesc_nvfp4(2 * BM, TN);
     static constexpr int CPW = PLAIN ? TN / 4 : 32;       // output columns per epilogue warp per tile
-    static constexpr int BOXW = MODE == 0 ? CPW : 32;     // store box width (columns)
+    static constexpr int BOXW = (MODE == 0 || MODE == 3) ? CPW : 32;  // store box width (columns)
     static constexpr int STG_BYTES = 32 * BOXW * 2;       // one staging box: 32 rows x BOXW bf16
     static constexpr bool STAGED = true;
     static constexpr bool TMA_STORE = true;               // false: coalesced warp stores from the staging box
@@ -128,9 +138,9 @@ struct Cfg {
 template <int MODE>
 struct __align__(1024) Smem {
     using C = Cfg<MODE>;
-    uint8_t a[C::STAGES][C::A_BYTES];
+    uint8_t a[C::A_SLOTS][C::A_BYTES];
     uint8_t b[C::STAGES][C::B_BYTES];
-    uint8_t sfa[C::STAGES][C::SFA_BYTES];
+    uint8_t sfa[C::A_SLOTS][C::SFA_BYTES];
     uint8_t sfb[C::STAGES][C::SFB_BYTES];
     uint8_t stg[C::NSTG > 0 ? C::NSTG : 1][C::NSTG > 0 ? C::STG_BYTES : 16];
     uint64_t full_a[C::STAGES];    // this CTA's A tile and scales landed
@@ -139,6 +149,7 @@ struct __align__(1024) Smem {
     uint64_t empty[C::STAGES];     // MMAs of the stage done (commit, multicast to the pair)
     uint64_t tmem_full[C::ACC_BUFS];   // accumulator ready (commit, multicast to the pair)
     uint64_t tmem_empty[C::ACC_BUFS];  // (even CTA) accumulator drained: one arrival per epilogue warp of the pair
+    uint64_t a_full[C::A_SLOTS];   // mode 3: K-stage of the resident A tile encoded (one arrival per epilogue warp)
     uint64_t drain;
     uint64_t never;                // no arrival ever: the time-out test's wait
     uint32_t tmem_base;
@@ -146,15 +157,18 @@ struct __align__(1024) Smem {
     int goff[MAX_G + 1];
     int gpoff[MAX_G + 1];
     int ppre[MAX_G + 1];           // units of m-tile pairs before each group
+    float ascale[BM];              // mode 3: the resident tile's row scales (alpha of D's rows)
 };
 static_assert(sizeof(Smem<0>) + 1024 <= 232448 && sizeof(Smem<1>) + 1024 <= 232448 &&
-              sizeof(Smem<2>) + 1024 <= 232448, "shared memory per CTA");
+              sizeof(Smem<2>) + 1024 <= 232448 && sizeof(Smem<3>) + 1024 <= 232448, "shared memory per CTA");
 // the two plain forms share the host-side tensor maps
 static_assert(Cfg<2>::ROWB == Cfg<0>::ROWB && Cfg<2>::ATOMS == Cfg<0>::ATOMS && Cfg<2>::TN == Cfg<0>::TN &&
               Cfg<2>::B_ROWS == Cfg<0>::B_ROWS && Cfg<2>::SFB_BLOCKS == Cfg<0>::SFB_BLOCKS, "plain forms");
 // the staging boxes start on 1024-byte boundaries (the TMA swizzle patterns repeat per 1024 bytes)
 static_assert(offsetof(Smem<0>, stg) % 1024 == 0 && offsetof(Smem<1>, stg) % 1024 == 0 &&
-              offsetof(Smem<2>, stg) % 1024 == 0, "staging alignment");
+              offsetof(Smem<2>, stg) % 1024 == 0 && offsetof(Smem<3>, stg) % 1024 == 0, "staging alignment");
+static_assert(Cfg<3>::ROWB == Cfg<0>::ROWB && Cfg<3>::TN == Cfg<0>::TN && Cfg<3>::B_ROWS == Cfg<0>::B_ROWS &&
+              Cfg<3>::BOXW == Cfg<0>::BOXW, "mode 3 shares mode 0's tensor maps");
 
 struct KParams {
     const uint8_t* a_sf;
@@ -173,10 +187,19 @@ struct KParams {
     float* c_debug;
     uint32_t* err;
     int stall;
+    // mode 3: the bf16 rows of D [M x K] and their amax (FC1's epilogue), and
+    // nullable copies of what the kernel encodes (codes [M x K/2], swizzled
+    // block scales of the padded rows, row scales [M]) for inspection
+    const __nv_bfloat16* d_in;
+    const float* d_amax;
+    uint8_t* q_codes;
+    uint8_t* q_sf;
+    float* q_scale;
 };
 
 struct Tile {
     int g, row0, rows, mt, nt;
+    int arows;  // rows of m-tile mt (the partner's when this CTA has none): the A rows it stages
 };
 
 // Unit u = (pair row pr, n-tile nt), nt fastest.  Pair row pr lies in the
@@ -199,7 +222,8 @@ __device__ __forceinline__ Tile decode_unit(const S& s, int G, int n_tiles, int 
     x.mt = none ? mt0 : mt0 + (int)rank;
     x.row0 = s.goff[lo] + (x.mt * BM - s.gpoff[lo]);
     const int end = s.goff[lo + 1];
-    x.rows = none ? 0 : (end - x.row0 < BM ? end - x.row0 : BM);
+    x.arows = end - x.row0 < BM ? end - x.row0 : BM;
+    x.rows = none ? 0 : x.arows;
     return x;
 }
 
@@ -340,6 +364,75 @@ __device__ __forceinline__ uint32_t swiglu_words(const uint32_t* v, uint64_t sca
     return mw;
 }
 
+// Mode 3: encode the A rows of one m-tile into the resident tile, by the 16
+// epilogue warps (wi = 0..15).  Rows row0 .. row0 + arows - 1 of D (K bf16
+// columns) take their outer scale from FC1's row amax; rows past arows
+// encode as zero.  Per K-stage kc: 16 lanes per row (lane j of a half-warp
+// takes the stage's 16-element block j), two rows per warp, four passes of
+// 32 rows.  Codes go to the stage's 128-byte rows in the 128B-swizzled
+// layout the TMA would have written (16-byte chunk c of row r at chunk
+// c ^ (r % 8)), block scales to the stage's 512-byte atoms (row r, block j:
+// byte (r % 32) 16 + (r / 32) 4 + j % 4 of atom j / 4), row scales to
+// ascale.  Each warp fences its writes to the async proxy and arrives on
+// a_full[kc].  The same block encode as the quantization kernels, so the
+// codes and scales are those of the separate requantization.
+template <class S>
+__device__ __forceinline__ void encode_a_tile(S& s, const KParams& p, int row0, int arows, int mt, int k_stages,
+                                              int wi, int lane) {
+    const int half = lane >> 4, b = lane & 15;
+    const int64_t sp4 = p.K / 64;
+    for (int kc = 0; kc < k_stages; ++kc) {
+#pragma unroll 2
+        for (int pass = 0; pass < 4; ++pass) {
+            const int r = pass * 32 + wi * 2 + half;
+            const bool valid = r < arows;
+            uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = make_uint4(0u, 0u, 0u, 0u);
+            float amax = 0.0f;
+            if (valid) {
+                const __nv_bfloat16* src = p.d_in + (int64_t)(row0 + r) * p.K + kc * 256 + b * 16;
+                asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                             : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z),
+                               "=r"(hi.w)
+                             : "l"(src));
+                amax = __ldg(p.d_amax + row0 + r);
+            }
+            const float s_g = outer_scale(amax, 2688.0f);  // 0 for a zero row
+            uint2 w = make_uint2(0u, 0u);
+            uint32_t sb = 0;
+            if (s_g != 0.0f) {
+                const float t = __fmul_rn(6.0f, s_g);
+                w = encode16(lo, hi, absmax16(lo, hi), s_g, t, rcp_rn(t), &sb);
+            }
+            *reinterpret_cast<uint2*>(s.a[kc] + r * 128 + (((b >> 1) ^ (r & 7)) << 4) + ((b & 1) << 3)) = w;
+            // the 4 blocks of a 64-column atom are 4 neighbouring lanes: one scale word
+            uint32_t word = sb;
+            word |= __shfl_down_sync(0xffffffffu, sb, 1) << 8;
+            word |= __shfl_down_sync(0xffffffffu, sb, 2) << 16;
+            word |= __shfl_down_sync(0xffffffffu, sb, 3) << 24;
+            if ((b & 3) == 0)
+                *reinterpret_cast<uint32_t*>(s.sfa[kc] + (b >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4) = word;
+            if (kc == 0 && b == 0) s.ascale[r] = valid ? s_g : 0.0f;
+            if (p.q_codes != nullptr) {  // inspection copies, in the separate requantization's layout
+                if (valid) *reinterpret_cast<uint2*>(p.q_codes + (int64_t)(row0 + r) * (p.K / 2) + kc * 128 + b * 8) = w;
+                if (valid && (b & 3) == 0)
+                    *reinterpret_cast<uint32_t*>(p.q_sf + sf_group_offset((int64_t)mt * BM + r, kc * 4 + (b >> 2), sp4)) =
+                        word;
+                if (valid && kc == 0 && b == 0) p.q_scale[row0 + r] = s_g;
+            }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&s.a_full[kc]));
+    }
+}
+
+// Mode 3: pull the D rows of an m-tile into L2 ahead of its encode.
+__device__ __forceinline__ void prefetch_a_rows(const KParams& p, int row0, int arows) {
+    const char* src = reinterpret_cast<const char*>(p.d_in + (int64_t)row0 * p.K);
+    const uint32_t bytes = (uint32_t)arows * (uint32_t)p.K * 2u;
+    for (uint32_t o = 0; o < bytes; o += 16384u) prefetch_l2(src + o, bytes - o < 16384u ? bytes - o : 16384u);
+}
+
 template <int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -377,12 +470,17 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             mbar_init(smem_u32(&s.tmem_full[i]), 1);
             mbar_init(smem_u32(&s.tmem_empty[i]), 2 * EPI_WARPS);
         }
+        if (C::QOL)
+            for (int i = 0; i < C::A_SLOTS; ++i) mbar_init(smem_u32(&s.a_full[i]), EPI_WARPS);
         mbar_init(smem_u32(&s.drain), 1);
         mbar_init(smem_u32(&s.never), 1);
         s.abort = 0;
         fence_barrier_init();
     }
-    if (warp == 0 && lane == 0) { prefetch_tmap(&tmA); prefetch_tmap(&tmO); }
+    if (warp == 0 && lane == 0) {
+        if (!C::QOL) prefetch_tmap(&tmA);
+        prefetch_tmap(&tmO);
+    }
     if (warp == PRODB_WARP && lane == 0) { prefetch_tmap(&tmB); prefetch_tmap(&tmSFB); }
     if (warp == 1) { tmem_alloc2(smem_u32(&s.tmem_base), TMEM_COLS); tmem_relinquish2(); }
     __syncthreads();
@@ -419,17 +517,25 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const int total = s.ppre[G] * n_tiles;
     const int k_atoms = p.K / 64;
     const int k_stages = (k_atoms + ATOMS - 1) / ATOMS;
+    // Unit order.  Modes 0-2 deal units round-robin (u = pair, pair + n_pairs,
+    // ...): the n-tiles of one m-tile pair run on neighbouring pairs at once
+    // and share its A rows in L2.  Mode 3 gives each pair whole m-tile pairs,
+    // all n-tiles back to back on the resident A tile.
+    const int u_first = C::QOL ? pair * n_tiles : pair;
+    auto u_next = [&](int u) {
+        return C::QOL ? ((u + 1) % n_tiles == 0 ? u + 1 + (n_pairs - 1) * n_tiles : u + 1) : u + n_pairs;
+    };
 
-    if (warp == 0 || warp == PRODB_WARP) {
+    if ((warp == 0 && !C::QOL) || warp == PRODB_WARP) {
         if (lane == 0) {
             // ------------------------------------------------------------ producers
             // warp 0: A rows + their scales; warp 22: B half + weight scales
-            const bool is_a = warp == 0;
+            const bool is_a = warp == 0 && !C::QOL;  // mode 3 has no A producer (warp 0 idles)
             uint64_t* full = is_a ? s.full_a : s.full_b;
             int stage = 0, issued = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int u = pair; u < total && ok; u += n_pairs) {
+            for (int u = u_first; u < total && ok; u = u_next(u)) {
                 const Tile x = decode_unit(s, G, n_tiles, u, rank);
                 // 128-row weight blocks of the tile: mode 1 takes 128 gate and
                 // 128 up rows of the expert (one per CTA), mode 0 the tile's
@@ -485,7 +591,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             bool ok = true;
             // the time-out test: a bounded wait for a phase that never completes
             if (p.stall) ok = mbar_wait_bounded_relaxed(smem_u32(&s.never), 0, abort, p.err);
-            for (int u = pair; u < total && ok; u += n_pairs, ++it) {
+            for (int u = u_first; u < total && ok; u = u_next(u), ++it) {
                 // accumulator it % ACC_BUFS, in its (it / ACC_BUFS)-th use
                 const int ab = ACC_BUFS == 1 ? 0 : (it & 1);
                 const uint32_t acc_phase = (uint32_t)(ACC_BUFS == 1 ? it : it >> 1) & 1u;
@@ -496,7 +602,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     tc_fence_after();
                     const int na = k_atoms - ks * ATOMS;
                     const uint32_t sfc = tmem + SF_COL + stage * SF_STAGE_COLS;
-                    const uint64_t ad = adesc0 + (uint64_t)((stage * A_BYTES) >> 4);
+                    const uint64_t ad = adesc0 + (uint64_t)(((C::QOL ? ks : stage) * A_BYTES) >> 4);
                     const uint64_t bd = bdesc0 + (uint64_t)((stage * B_BYTES) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < ATOMS; ++kk) {
@@ -515,7 +621,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             tc_commit2_mc(smem_u32(&s.drain), 1);
             mbar_wait_drain(smem_u32(&s.drain), 0);
         }
-    } else if (warp < EPI_WARP0) {
+    } else if (warp >= 2 && warp < EPI_WARP0) {
         // ---------------------------------------------------------------- scale writers
         // Warp w writes TMEM lane quarter w % 4.  Each scale atom (32 lines
         // of 16 bytes; line i holds the 4 scales of rows i, i+32, i+64, i+96)
@@ -527,17 +633,20 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        for (int u = pair; u < total && ok; u += n_pairs) {
+        int it = 0;
+        for (int u = u_first; u < total && ok; u = u_next(u), ++it) {
             for (int ks = 0; ks < k_stages; ++ks) {
-                if (!mbar_wait_bounded(smem_u32(&s.full_a[stage]), phase, abort, p.err) ||
-                    !mbar_wait_bounded(smem_u32(&s.full_b[stage]), phase, abort, p.err)) { ok = false; break; }
+                // mode 3: stage ks of the resident A tile, encoded for this unit's m-tile (the it / n_tiles-th)
+                const bool a_in = C::QOL ? mbar_wait_bounded(smem_u32(&s.a_full[ks]), (uint32_t)(it / n_tiles) & 1u, abort, p.err)
+                                         : mbar_wait_bounded(smem_u32(&s.full_a[stage]), phase, abort, p.err);
+                if (!a_in || !mbar_wait_bounded(smem_u32(&s.full_b[stage]), phase, abort, p.err)) { ok = false; break; }
                 const uint32_t sfc = lane_addr + SF_COL + stage * SF_STAGE_COLS;
                 // the stage's SFA columns (4 per atom) and SFB columns (4 per atom and 128-row
                 // block) are contiguous runs: one wide store each
                 uint32_t fa[4 * ATOMS], fb[4 * ATOMS * SFB_BLOCKS];
 #pragma unroll
                 for (int kk = 0; kk < ATOMS; ++kk) {
-                    const uint4 a = *reinterpret_cast<const uint4*>(s.sfa[stage] + kk * 512 + lane * 16);
+                    const uint4 a = *reinterpret_cast<const uint4*>(s.sfa[C::QOL ? ks : stage] + kk * 512 + lane * 16);
                     fa[4 * kk] = a.x; fa[4 * kk + 1] = a.y; fa[4 * kk + 2] = a.z; fa[4 * kk + 3] = a.w;
 #pragma unroll
                     for (int hh = 0; hh < SFB_BLOCKS; ++hh) {
@@ -559,7 +668,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             }
         }
         if (!ok && lane == 0) raise_abort(&s.abort, rank);
-    } else if (warp < PRODB_WARP) {
+    } else if (warp >= EPI_WARP0 && warp < PRODB_WARP) {
         // ---------------------------------------------------------------- epilogue
         // Each warp copies its 32 rows x 64 accumulator columns into
         // registers (mode 1: 32 gate and the matching 32 up columns) and
@@ -572,7 +681,19 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         bool ok = true;
         int nbox = 0;  // staged boxes this warp has stored
         int it = 0;    // tiles of this CTA so far
-        for (int u = pair; u < total; u += n_pairs, ++it) {
+        const int wi = warp - EPI_WARP0;
+        float sa_m = 0.0f;  // mode 3: this thread's row scale in the current m-tile
+        if (C::QOL && u_first < total) {
+            // the pair's first m-tile: encode it, and pull the next one's rows into L2
+            const Tile x0 = decode_unit(s, G, n_tiles, u_first, rank);
+            encode_a_tile(s, p, x0.row0, x0.arows, x0.mt, k_stages, wi, lane);
+            const int un = u_first + n_pairs * n_tiles;
+            if (wi == 0 && lane == 0 && un < total) {
+                const Tile xn = decode_unit(s, G, n_tiles, un, rank);
+                prefetch_a_rows(p, xn.row0, xn.arows);
+            }
+        }
+        for (int u = u_first; u < total; u = u_next(u), ++it) {
             const int ab = ACC_BUFS == 1 ? 0 : (it & 1);
             const uint32_t acc_phase = (uint32_t)(ACC_BUFS == 1 ? it : it >> 1) & 1u;
             const Tile x = decode_unit(s, G, n_tiles, u, rank);
@@ -580,7 +701,22 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             const bool valid = rl < x.rows;
             const int64_t row = (int64_t)x.row0 + rl;
             // scales are fetched before the wait so their latency hides under the MMAs
-            const float sa = valid ? __ldg(p.a_scale + row) : 0.0f;
+            float sa;
+            if (C::QOL) {
+                // the m-tile's first unit: every warp's encode of it is complete (and its
+                // row scales visible) once a_full[0] has its phase; the scale stays in a
+                // register for the m-tile's units, as the next encode rewrites ascale
+                if (x.nt == 0) {
+                    if (!mbar_wait_bounded(smem_u32(&s.a_full[0]), (uint32_t)(it / n_tiles) & 1u, abort, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    sa_m = s.ascale[rl];
+                }
+                sa = valid ? sa_m : 0.0f;
+            } else {
+                sa = valid ? __ldg(p.a_scale + row) : 0.0f;
+            }
             const float sbw = __ldg(p.b_scale + x.g);
             const float prob = (valid && p.row_prob) ? __ldg(p.row_prob + row) : 1.0f;
             if (!mbar_wait_bounded_relaxed(smem_u32(&s.tmem_full[ab]), acc_phase, abort, p.err)) { ok = false; break; }
@@ -601,7 +737,25 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             // the pair have theirs in registers.  A warp arrives for tile t + 1
             // only after tile t + 1's commit, which follows that completion.
             if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&s.tmem_empty[ab]), 0));
-            if (x.rows == 0) continue;  // the odd CTA of a group's last pair: nothing to store
+            // Mode 3, the m-tile's last unit: its MMAs (done: tmem_full) no longer read
+            // the resident tile, so the pair's next m-tile is encoded over it.  Run
+            // after this unit's outputs have left the registers (staged and stored).
+            auto encode_next = [&]() {
+                if (!C::QOL || x.nt != n_tiles - 1) return;
+                const int un = u_next(u);
+                if (un >= total) return;
+                const Tile xn = decode_unit(s, G, n_tiles, un, rank);
+                encode_a_tile(s, p, xn.row0, xn.arows, xn.mt, k_stages, wi, lane);
+                const int un2 = un + n_pairs * n_tiles;
+                if (wi == 0 && lane == 0 && un2 < total) {
+                    const Tile x2 = decode_unit(s, G, n_tiles, un2, rank);
+                    prefetch_a_rows(p, x2.row0, x2.arows);
+                }
+            };
+            if (x.rows == 0) {  // the odd CTA of a group's last pair: nothing to store
+                encode_next();
+                continue;
+            }
             const float scale = __fmul_rn(sa, sbw);
             const uint64_t scale2 = f2(scale, scale);
             // all 32 rows of this warp inside the tile's group: TMA store; else direct
@@ -646,6 +800,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     atomicMax(reinterpret_cast<unsigned int*>(p.amax_out + row), __float_as_uint(mb));
                 }
             }
+            encode_next();
         }
         if (!ok && lane == 0) raise_abort(&s.abort, rank);
         if (C::STAGED && lane == 0) bulk_wait_all();  // this warp's tensor stores are complete before exit
@@ -804,15 +959,22 @@ int device_sm_count() {
 
 cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
     if (g.M <= 0) return cudaSuccess;
+    const bool qol = g.mode == 3;
+    if (qol && (g.goff == nullptr || g.d_in == nullptr || g.d_amax == nullptr || g.K % 256 != 0 ||
+                g.K / 256 > Cfg<3>::KCH || g.N % 256 != 0 || g.N / 256 < 2))
+        return cudaErrorInvalidValue;
+    const int map_mode = g.mode == 1 ? 1 : 0;  // modes 0, 2 and 3 share the plain tensor maps
     CUtensorMap ta, tb, tsfb, to;
-    if (!make_codes_map(&ta, g.a_codes, g.M, g.K / 2, g.mode, BM)) return cudaErrorInvalidValue;
-    const int b_rows = g.mode == 0 ? Cfg<0>::B_ROWS : Cfg<1>::B_ROWS;
+    const int b_rows = map_mode == 0 ? Cfg<0>::B_ROWS : Cfg<1>::B_ROWS;
     // plain GEMMs with long K loops (4 or more stages of 256) take the 5-stage form
     const int plain_mode = (g.K / 256 >= 4) ? 2 : 0;
-    if (!make_codes_map(&tb, g.b_codes, (int64_t)g.G * g.N, g.K / 2, g.mode, b_rows)) return cudaErrorInvalidValue;
-    if (!make_sfb_map(&tsfb, g.b_sf, g.goff ? g.G : 1, g.N, g.K, g.mode)) return cudaErrorInvalidValue;
+    if (!make_codes_map(&tb, g.b_codes, (int64_t)g.G * g.N, g.K / 2, map_mode, b_rows)) return cudaErrorInvalidValue;
+    // mode 3 has no A tensor (the kernel encodes A): its map argument repeats B's, unused
+    if (qol) ta = tb;
+    else if (!make_codes_map(&ta, g.a_codes, g.M, g.K / 2, map_mode, BM)) return cudaErrorInvalidValue;
+    if (!make_sfb_map(&tsfb, g.b_sf, g.goff ? g.G : 1, g.N, g.K, map_mode)) return cudaErrorInvalidValue;
     const int64_t out_cols = g.mode == 1 ? g.N / 2 : g.N;
-    const int box_cols = g.mode == 0 ? (plain_mode == 2 ? Cfg<2>::BOXW : Cfg<0>::BOXW) : Cfg<1>::BOXW;
+    const int box_cols = g.mode == 1 ? Cfg<1>::BOXW : (g.mode == 0 && plain_mode == 2 ? Cfg<2>::BOXW : Cfg<0>::BOXW);
     if (!make_out_map(&to, g.out, g.M, out_cols, g.ldo, box_cols)) return cudaErrorInvalidValue;
     KParams p;
     p.a_sf = g.a_sf;
@@ -833,10 +995,16 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
     p.c_debug = g.c_debug;
     p.err = g.err;
     p.stall = g.stall;
+    p.d_in = reinterpret_cast<const __nv_bfloat16*>(g.d_in);
+    p.d_amax = g.d_amax;
+    p.q_codes = g.q_codes;
+    p.q_sf = g.q_sf;
+    p.q_scale = g.q_scale;
     const int num_sms = g.num_sms > 0 ? g.num_sms : 148;
     // dense calls: no more pairs than units of work (m-tile pairs x n-tiles)
-    const int tn = g.mode == 0 ? Cfg<0>::TN : Cfg<1>::TN;
+    const int tn = g.mode == 1 ? Cfg<1>::TN : Cfg<0>::TN;
     const int64_t dense_units = g.goff == nullptr ? ((g.M + BM - 1) / BM + 1) / 2 * (g.N / tn) : 0;
+    if (qol) return launch_mode<3>(ta, tb, tsfb, to, p, num_sms, 0, stream);
     if (g.mode == 0 && plain_mode == 2) return launch_mode<2>(ta, tb, tsfb, to, p, num_sms, dense_units, stream);
     if (g.mode == 0) return launch_mode<0>(ta, tb, tsfb, to, p, num_sms, dense_units, stream);
     return launch_mode<1>(ta, tb, tsfb, to, p, num_sms, dense_units, stream);

@@ -60,7 +60,7 @@ struct GemmLaunch {
     int N, K, G;
     const int* goff;       // nullable (dense: one group of M rows)
     const int* gpoff;
-    int mode;              // 0 plain, 1 SwiGLU
+    int mode;              // 0 plain, 1 SwiGLU, 3 plain with A encoded from bf16 rows in the kernel
     void* out;             // bf16
     int64_t ldo;
     float* amax_out;       // mode 1
@@ -69,6 +69,16 @@ struct GemmLaunch {
     uint32_t* err;         // nullable
     int num_sms;
     int stall;             // test of the time-out path: the MMA thread waits on a barrier nothing arrives at
+    // mode 3 (plain out, A encoded in the kernel from bf16 rows; grouped, K a
+    // multiple of 256 up to 768, N a multiple of 256 of at least 512): D
+    // [M x K] bf16 and its row amax [M] stand in for a_codes / a_sf /
+    // a_scale; q_codes / q_sf / q_scale (nullable) receive copies of the
+    // encoded codes, swizzled padded-row block scales and row scales
+    const void* d_in;
+    const float* d_amax;
+    uint8_t* q_codes;
+    uint8_t* q_sf;
+    float* q_scale;
 };
 cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t stream);
 

@@ -125,6 +125,10 @@ def test_moe_rejects_bad_arguments(L):
     assert call(ws=4096 + 16) == -3
     assert call(x=None) == -1
     assert call(T=0) == -1
+    for bad in (-1, 3):  # moe_options.fc2_requant outside MOE_REQUANT_AUTO .. MOE_REQUANT_IN_FC2
+        opt.fc2_requant = bad
+        assert call() == -1
+    opt.fc2_requant = 0
 
 
 def test_quantize_grouped_rejects_bad_arguments(L):
