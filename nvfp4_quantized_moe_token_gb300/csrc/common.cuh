@@ -182,9 +182,14 @@ __device__ __forceinline__ bool mbar_wait_bounded_relaxed(uint32_t bar, uint32_t
         }
     }
 }
-// L2 prefetch of `bytes` (a multiple of 16) from a 16-byte aligned global address.
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src), "r"(bytes) : "memory");
+// L2 prefetch of `bytes` (a multiple of 16) from a 16-byte aligned global
+// address, marked to be evicted last: the lines must survive until they are
+// read, while other streams pass through L2.
+__device__ __forceinline__ void prefetch_l2_keep(const void* src, uint32_t bytes) {
+    asm volatile("{\n\t.reg .b64 pol;\n\t"
+                 "createpolicy.fractional.L2::evict_last.b64 pol, 1.0;\n\t"
+                 "cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, pol;\n\t}"
+                 :: "l"(src), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");

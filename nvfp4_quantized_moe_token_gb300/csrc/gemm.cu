@@ -381,27 +381,37 @@ __device__ __forceinline__ void encode_a_tile(S& s, const KParams& p, int row0, 
                                               int wi, int lane) {
     const int half = lane >> 4, b = lane & 15;
     const int64_t sp4 = p.K / 64;
+    uint64_t pol;  // the rows are read once: first out of L2
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
     for (int kc = 0; kc < k_stages; ++kc) {
-#pragma unroll 2
+        // the stage's four passes load before any encodes: four loads in flight per lane
+        uint4 lo[4], hi[4];
+        float amax[4];
+#pragma unroll
+        for (int pass = 0; pass < 4; ++pass) {
+            const int r = pass * 32 + wi * 2 + half;
+            lo[pass] = make_uint4(0u, 0u, 0u, 0u);
+            hi[pass] = make_uint4(0u, 0u, 0u, 0u);
+            amax[pass] = 0.0f;
+            if (r < arows) {
+                const __nv_bfloat16* src = p.d_in + (int64_t)(row0 + r) * p.K + kc * 256 + b * 16;
+                asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8], %9;"
+                             : "=r"(lo[pass].x), "=r"(lo[pass].y), "=r"(lo[pass].z), "=r"(lo[pass].w),
+                               "=r"(hi[pass].x), "=r"(hi[pass].y), "=r"(hi[pass].z), "=r"(hi[pass].w)
+                             : "l"(src), "l"(pol));
+                amax[pass] = __ldg(p.d_amax + row0 + r);
+            }
+        }
+#pragma unroll
         for (int pass = 0; pass < 4; ++pass) {
             const int r = pass * 32 + wi * 2 + half;
             const bool valid = r < arows;
-            uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = make_uint4(0u, 0u, 0u, 0u);
-            float amax = 0.0f;
-            if (valid) {
-                const __nv_bfloat16* src = p.d_in + (int64_t)(row0 + r) * p.K + kc * 256 + b * 16;
-                asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-                             : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z),
-                               "=r"(hi.w)
-                             : "l"(src));
-                amax = __ldg(p.d_amax + row0 + r);
-            }
-            const float s_g = outer_scale(amax, 2688.0f);  // 0 for a zero row
+            const float s_g = outer_scale(amax[pass], 2688.0f);  // 0 for a zero row
             uint2 w = make_uint2(0u, 0u);
             uint32_t sb = 0;
             if (s_g != 0.0f) {
                 const float t = __fmul_rn(6.0f, s_g);
-                w = encode16(lo, hi, absmax16(lo, hi), s_g, t, rcp_rn(t), &sb);
+                w = encode16(lo[pass], hi[pass], absmax16(lo[pass], hi[pass]), s_g, t, rcp_rn(t), &sb);
             }
             *reinterpret_cast<uint2*>(s.a[kc] + r * 128 + (((b >> 1) ^ (r & 7)) << 4) + ((b & 1) << 3)) = w;
             // the 4 blocks of a 64-column atom are 4 neighbouring lanes: one scale word
@@ -430,7 +440,7 @@ __device__ __forceinline__ void encode_a_tile(S& s, const KParams& p, int row0, 
 __device__ __forceinline__ void prefetch_a_rows(const KParams& p, int row0, int arows) {
     const char* src = reinterpret_cast<const char*>(p.d_in + (int64_t)row0 * p.K);
     const uint32_t bytes = (uint32_t)arows * (uint32_t)p.K * 2u;
-    for (uint32_t o = 0; o < bytes; o += 16384u) prefetch_l2(src + o, bytes - o < 16384u ? bytes - o : 16384u);
+    for (uint32_t o = 0; o < bytes; o += 16384u) prefetch_l2_keep(src + o, bytes - o < 16384u ? bytes - o : 16384u);
 }
 
 template <int MODE>
