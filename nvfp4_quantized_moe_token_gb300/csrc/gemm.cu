@@ -39,15 +39,15 @@
 //                occupies the tensor pipe for ~55-80 cycles whatever its size;
 //                tcgen05.st runs on the warps.)
 //   warps 6-21   epilogue: each warp copies its 32 rows x 64 accumulator
-//                columns into registers and arrives on a barrier of its CTA;
-//                warp 6 waits for all 16 and releases the CTA's half of TMEM
-//                with one arrival on the even CTA's barrier (the next tile's
-//                MMAs start), then each warp
-//                scales and either converts to bf16 (mode 0) or computes
-//                SwiGLU -> bf16 D + row amax (mode 1).  Outputs leave
-//                through a per-warp shared-memory box of 32 rows x 32 columns
-//                and a TMA tensor store; a warp whose 32 rows straddle the end
-//                of an expert group stores its valid rows directly.
+//                columns into registers and releases them with its own
+//                arrival on the even CTA's barrier (the next tile's MMAs
+//                start once all 32 warps of the pair have theirs), then
+//                scales and either converts to bf16 (modes 0, 2, 3) or
+//                computes SwiGLU -> bf16 D + row amax (mode 1).  Outputs leave
+//                through a per-warp shared-memory box and a TMA tensor store;
+//                a warp whose 32 rows straddle the end of an expert group
+//                stores its valid rows directly.  In mode 3 these warps also
+//                encode the resident A tile (and warp 0 has no role).
 // Work units are (pair of m-tiles of one group, n-tile), n fastest, so pairs
 // running at the same time share the A rows and one expert's weights in L2.
 // A group with an odd number of m-tiles ends in a unit whose odd CTA has no
