@@ -91,6 +91,20 @@ def test_in_fc2_ragged_layers(T, E, k, H, F, seed):
     _check(run, lay)
 
 
+def test_in_fc2_with_the_router_weight_at_fc1():
+    """The pages' weighted-SwiGLU placement (moe_options.weight_at_fc1): D
+    carries the router weight before its amax and requantization, which FC2
+    then performs; same bits as the separate launch."""
+    rng = np.random.default_rng(5)
+    T, E, k, H, F = 900, 64, 8, 512, 512
+    d = {"x": workloads.gaussian_bf16(rng, (T, H)), "logits": rng.standard_normal((T, E), dtype=np.float32),
+         "bias": rng.standard_normal(E, dtype=np.float32),
+         "w1": workloads.gaussian_bf16(rng, (E, 2 * F, H), std=0.02),
+         "w2": workloads.gaussian_bf16(rng, (E, H, F), std=0.02)}
+    run, lay = _layer(d, E, k, F)
+    _check(run, lay, weight_at_fc1=True)
+
+
 def test_in_fc2_falls_back_where_it_does_not_apply():
     """Four-over-six activations and F = 640 (not a multiple of 256) take the
     separate launch under MOE_REQUANT_IN_FC2: same bits, requantized slots
