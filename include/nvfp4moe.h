@@ -278,6 +278,15 @@ typedef struct moe_options {
      *     launch.  The workspace's requantized copies (a2_codes, a2_sf,
      *     a2_scale) are then written only on request (moe_debug.requant_copy). */
     int fc2_requant;
+    /* 0: the router-weighted combine is its own launch after FC2 (default).
+     * 1: FC2's epilogue does it: each 64-column block of a token's output is
+     * summed, in slot order, by the unit that writes the last of the token's
+     * k rows of that block (arrival counters in the workspace), reading the
+     * other rows back from Y2.  Bit-identical to the separate combine (the
+     * same fp32 fused multiply-adds in the same order); Y2 is still written.
+     * Only with the separate requantization (fc2_requant other than
+     * MOE_REQUANT_IN_FC2) and F up to 768; otherwise the separate combine. */
+    int fc2_combine;
 } moe_options;
 
 #define MOE_REQUANT_AUTO 0
@@ -344,6 +353,7 @@ typedef struct moe_workspace_layout {
     size_t a2_sf;        /* swizzled [Rp x F/16], padded per expert like a1_sf */
     size_t a2_scale;     /* fp32 [R] */
     size_t y2;           /* bf16 [R x H] FC2 output in expert order */
+    size_t comb_cnt;     /* int32 [T x H/64] arrival counters of the combine inside FC2 */
 } moe_workspace_layout;
 
 /* Fill *layout for the given sizes; returns 0, or NVFP4_ESHAPE /
@@ -396,7 +406,7 @@ NVFP4_API int moe_expert_forward(const void* x_bf16, int64_t T, int64_t H,
  *   until the process exits.  Sizes whose workspace
  *   (moe_expert_workspace()) exceeds 32 MiB are rejected with
  *   NVFP4_EWORKSPACE and a message; at hidden 2048, FFN 768, 128 experts,
- *   top-8 that is more than 518 tokens.
+ *   top-8 that is more than 516 tokens.
  *   The first call on each device looks the array's device address up
  *   (cudaGetSymbolAddress) with that device current, so make it before any
  *   stream capture.  Nothing is allocated, by this call or later ones.  The

@@ -25,7 +25,8 @@ class _Tensor(ctypes.Structure):
 
 
 class _Options(ctypes.Structure):
-    _fields_ = [("weight_at_fc1", ctypes.c_int), ("four_over_six", ctypes.c_int), ("fc2_requant", ctypes.c_int)]
+    _fields_ = [("weight_at_fc1", ctypes.c_int), ("four_over_six", ctypes.c_int), ("fc2_requant", ctypes.c_int),
+                ("fc2_combine", ctypes.c_int)]
 
 
 class _Debug(ctypes.Structure):
@@ -38,7 +39,7 @@ STAGES = ["quantize", "route", "fc1", "requant", "fc2", "combine"]
 
 LAYOUT_FIELDS = ["total", "err", "ids", "weights", "row_weights", "counts", "offsets", "padded_offsets",
                  "perm", "inv", "chunk_counts", "xq_codes", "xq_sf", "xq_scale", "a1_codes", "a1_sf",
-                 "a1_scale", "d", "amax2", "a2_codes", "a2_sf", "a2_scale", "y2"]
+                 "a1_scale", "d", "amax2", "a2_codes", "a2_sf", "a2_scale", "y2", "comb_cnt"]
 
 
 class _Layout(ctypes.Structure):
@@ -257,12 +258,14 @@ def moe_workspace_layout(T, H, F, E, topk):
 
 def moe_expert_forward(x, logits, bias, w1q, w2q, F, topk, weight_at_fc1=False, out=None,
                        ws=None, fc1_debug=None, stage_events=None, four_over_six=None, stream=None,
-                       debug_stall_fc1=False, fc2_requant=None, requant_copy=False):
+                       debug_stall_fc1=False, fc2_requant=None, requant_copy=False, fc2_combine=False):
     """One W4A4 MoE expert layer on the device.  Returns (out bf16 [T, H], ws).
     four_over_six (None, 'mse', 'mae'): four-over-six scaling of the activations.
     fc2_requant (None: the library's choice, 'separate', 'in_fc2'): where D is
     requantized (moe_options.fc2_requant); requant_copy: with 'in_fc2', also
     write the encoded D to the workspace's a2 slots (moe_debug.requant_copy).
+    fc2_combine: the router-weighted combine inside FC2's epilogue
+    (moe_options.fc2_combine).
     debug_stall_fc1: test of the time-out path (moe_debug.stall_fc1): FC1's
     bounded wait runs out, DEVERR_TIMEOUT is set in the workspace's error
     word, the outputs are undefined.
@@ -278,7 +281,8 @@ def moe_expert_forward(x, logits, bias, w1q, w2q, F, topk, weight_at_fc1=False, 
     if out is None:
         out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
     a, b = w1q.c(), w2q.c()
-    opt = _Options(1 if weight_at_fc1 else 0, FOUR_OVER_SIX[four_over_six], FC2_REQUANT[fc2_requant])
+    opt = _Options(1 if weight_at_fc1 else 0, FOUR_OVER_SIX[four_over_six], FC2_REQUANT[fc2_requant],
+                   1 if fc2_combine else 0)
     evs = None
     if stage_events is not None:
         assert len(stage_events) == len(STAGES) + 1

@@ -351,6 +351,7 @@ int moe_expert_workspace_layout(int64_t T, int64_t H, int64_t F, int E, int topk
     L->a2_sf = take(Rp * ((F / 16 + 3) / 4 * 4));
     L->a2_scale = take(4 * R);
     L->y2 = take(2 * R * H);
+    L->comb_cnt = take(4 * T * (H / 64));
     L->total = o;
     return ok();
 }
@@ -391,6 +392,8 @@ int moe_expert_forward(const void* x_bf16, int64_t T, int64_t H, const float* ro
     const int requant = opt != nullptr ? opt->fc2_requant : MOE_REQUANT_AUTO;
     if (requant < MOE_REQUANT_AUTO || requant > MOE_REQUANT_IN_FC2)
         return fail(NVFP4_EINVAL, "moe: fc2_requant must be MOE_REQUANT_AUTO, _SEPARATE or _IN_FC2");
+    const int comb_opt = opt != nullptr ? opt->fc2_combine : 0;
+    if (comb_opt != 0 && comb_opt != 1) return fail(NVFP4_EINVAL, "moe: fc2_combine must be 0 or 1");
     if (sm_count() <= 0) return fail(NVFP4_ELAUNCH, "moe: no CUDA device");
     const bool at_fc1 = opt != nullptr && opt->weight_at_fc1 != 0;
     const int fos = fos_of(fos_flags);
@@ -451,6 +454,14 @@ int moe_expert_forward(const void* x_bf16, int64_t T, int64_t H, const float* ro
     r.a1_scale = reinterpret_cast<float*>(at(L.a1_scale));
     r.amax2 = reinterpret_cast<float*>(at(L.amax2));
     r.row_w = at_fc1 ? reinterpret_cast<float*>(at(L.row_weights)) : nullptr;
+    // the requantization inside FC2 (plain NVFP4, F a multiple of 256 up to 768,
+    // H >= 512) and the combine inside FC2's epilogue (FC2 on its 4-stage plain
+    // form, F < 1024, with the separate requantization); the scatter zeroes the
+    // combine's arrival counters
+    const bool in_fc2 = requant == MOE_REQUANT_IN_FC2 && fos == 0 && F % 256 == 0 && F <= 768 && H >= 512;
+    const bool comb_in_fc2 = comb_opt == 1 && !in_fc2 && F < 1024;
+    r.comb_cnt = comb_in_fc2 ? reinterpret_cast<int*>(at(L.comb_cnt)) : nullptr;
+    r.comb_blocks = (int)(H / 64);
 
     if ((e = nvfp4::launch_quantize_topk(qx, r, s)) != cudaSuccess)
         return fail(NVFP4_ELAUNCH, "moe quantize + top-k: %s", cudaGetErrorString(e));
@@ -485,8 +496,7 @@ int moe_expert_forward(const void* x_bf16, int64_t T, int64_t H, const float* ro
     if ((e = mark()) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe event: %s", cudaGetErrorString(e));
 
     // 4. requantize D per row, reusing the epilogue's amax: a separate launch,
-    //    or inside FC2 (plain NVFP4, F a multiple of 256 up to 768, H >= 512)
-    const bool in_fc2 = requant == MOE_REQUANT_IN_FC2 && fos == 0 && F % 256 == 0 && F <= 768 && H >= 512;
+    //    or inside FC2 (in_fc2, decided above)
     nvfp4::QuantLaunch q2{};
     q2.x = at(L.d);
     q2.ld = F;
@@ -520,7 +530,15 @@ int moe_expert_forward(const void* x_bf16, int64_t T, int64_t H, const float* ro
     g2.G = E;
     g2.goff = r.off;
     g2.gpoff = r.poff;
-    g2.mode = in_fc2 ? 3 : 0;
+    g2.mode = in_fc2 ? 3 : (comb_in_fc2 ? 4 : 0);
+    if (comb_in_fc2) {
+        g2.perm = r.perm;
+        g2.inv = r.inv;
+        g2.cw = at_fc1 ? nullptr : r.w;
+        g2.cout = out_bf16;
+        g2.ccnt = r.comb_cnt;
+        g2.k_top = topk;
+    }
     if (in_fc2) {
         g2.d_in = at(L.d);
         g2.d_amax = reinterpret_cast<const float*>(at(L.amax2));
@@ -546,7 +564,8 @@ int moe_expert_forward(const void* x_bf16, int64_t T, int64_t H, const float* ro
     c.H = H;
     c.k = topk;
     c.out = out_bf16;
-    if ((e = nvfp4::launch_combine(c, s)) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe combine: %s", cudaGetErrorString(e));
+    if (!comb_in_fc2 && (e = nvfp4::launch_combine(c, s)) != cudaSuccess)
+        return fail(NVFP4_ELAUNCH, "moe combine: %s", cudaGetErrorString(e));
     if ((e = mark()) != cudaSuccess) return fail(NVFP4_ELAUNCH, "moe event: %s", cudaGetErrorString(e));
     return ok();
 }

@@ -112,7 +112,8 @@ struct Cfg {
     static constexpr int SFB_BLOCKS = TN / 128;         // 128-row weight-scale blocks per tile
     static constexpr bool PLAIN = MODE != 1;            // modes 0, 2 and 3: plain bf16 out
     static constexpr bool QOL = MODE == 3;              // A quantized on load, resident across n-tiles
-    static constexpr int STAGES = (MODE == 0 || MODE == 3) ? 4 : 5;
+    static constexpr bool COMB = MODE == 4;             // mode 0 plus the combine in the epilogue
+    static constexpr int STAGES = (MODE == 0 || MODE == 3 || MODE == 4) ? 4 : 5;
     static constexpr int KCH = 3;                       // mode 3: K-stages of the resident A tile (K <= 768)
     static constexpr int A_SLOTS = QOL ? KCH : STAGES;  // A slots: the ring, or the resident tile's stages
     static constexpr int NBUF = 1;                      // staging boxes per epilogue warp
@@ -126,7 +127,7 @@ struct Cfg {
     static constexpr uint32_t SF_STAGE_COLS = 4 * ATOMS * (1 + SFB_BLOCKS);  // SFA 4 + SFB 4 per block, per atom
     static constexpr uint32_t IDESC = idesc_nvfp4(2 * BM, TN);
     static constexpr int CPW = PLAIN ? TN / 4 : 32;       // output columns per epilogue warp per tile
-    static constexpr int BOXW = (MODE == 0 || MODE == 3) ? CPW : 32;  // store box width (columns)
+    static constexpr int BOXW = (MODE == 0 || MODE == 3 || MODE == 4) ? CPW : 32;  // store box width (columns)
     static constexpr int STG_BYTES = 32 * BOXW * 2;       // one staging box: 32 rows x BOXW bf16
     static constexpr bool STAGED = true;
     static constexpr bool TMA_STORE = true;               // false: coalesced warp stores from the staging box
@@ -160,7 +161,8 @@ struct __align__(1024) Smem {
     float ascale[BM];              // mode 3: the resident tile's row scales (alpha of D's rows)
 };
 static_assert(sizeof(Smem<0>) + 1024 <= 232448 && sizeof(Smem<1>) + 1024 <= 232448 &&
-              sizeof(Smem<2>) + 1024 <= 232448 && sizeof(Smem<3>) + 1024 <= 232448, "shared memory per CTA");
+              sizeof(Smem<2>) + 1024 <= 232448 && sizeof(Smem<3>) + 1024 <= 232448 &&
+              sizeof(Smem<4>) + 1024 <= 232448, "shared memory per CTA");
 // the two plain forms share the host-side tensor maps
 static_assert(Cfg<2>::ROWB == Cfg<0>::ROWB && Cfg<2>::ATOMS == Cfg<0>::ATOMS && Cfg<2>::TN == Cfg<0>::TN &&
               Cfg<2>::B_ROWS == Cfg<0>::B_ROWS && Cfg<2>::SFB_BLOCKS == Cfg<0>::SFB_BLOCKS, "plain forms");
@@ -168,7 +170,9 @@ static_assert(Cfg<2>::ROWB == Cfg<0>::ROWB && Cfg<2>::ATOMS == Cfg<0>::ATOMS && 
 static_assert(offsetof(Smem<0>, stg) % 1024 == 0 && offsetof(Smem<1>, stg) % 1024 == 0 &&
               offsetof(Smem<2>, stg) % 1024 == 0 && offsetof(Smem<3>, stg) % 1024 == 0, "staging alignment");
 static_assert(Cfg<3>::ROWB == Cfg<0>::ROWB && Cfg<3>::TN == Cfg<0>::TN && Cfg<3>::B_ROWS == Cfg<0>::B_ROWS &&
-              Cfg<3>::BOXW == Cfg<0>::BOXW, "mode 3 shares mode 0's tensor maps");
+              Cfg<3>::BOXW == Cfg<0>::BOXW && Cfg<4>::ROWB == Cfg<0>::ROWB && Cfg<4>::TN == Cfg<0>::TN &&
+              Cfg<4>::B_ROWS == Cfg<0>::B_ROWS && Cfg<4>::BOXW == Cfg<0>::BOXW &&
+              offsetof(Smem<4>, stg) % 1024 == 0, "modes 3 and 4 share mode 0's tensor maps");
 
 struct KParams {
     const uint8_t* a_sf;
@@ -195,6 +199,13 @@ struct KParams {
     uint8_t* q_codes;
     uint8_t* q_sf;
     float* q_scale;
+    // mode 4: the router-weighted combine in the epilogue
+    const int* perm;
+    const int* inv;
+    const float* cw;
+    __nv_bfloat16* cout;
+    int* ccnt;
+    int k_top;
 };
 
 struct Tile {
@@ -433,6 +444,54 @@ __device__ __forceinline__ void encode_a_tile(S& s, const KParams& p, int row0, 
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&s.a_full[kc]));
+    }
+}
+
+// Mode 4: the router-weighted combine of the tokens whose k-th and last
+// output row of one 64-column block this warp has just written.  Each row of
+// the block counts its arrival on the token's counter for the block; the
+// arrival that brings it to k (whichever unit that is) sums the token's k
+// rows of that block, read back from Y2, in slot order -- the same fp32
+// fused multiply-adds in the same order as the combine kernel, so the output
+// is bit-identical and independent of which unit arrives last.  The warp's
+// own writes are complete and ordered before its counts (bulk wait, proxy
+// and gpu fences); the last arriver fences again before reading.  Up to four
+// completed tokens at a time, eight lanes each, 8 columns per lane.
+__device__ __forceinline__ void combine_completed(const KParams& p, bool valid, int64_t row, int blk, int lane) {
+    const int nblk = p.N >> 6;
+    bool last = false;
+    int tok = 0;
+    if (valid) {
+        tok = __ldg(p.perm + row) / p.k_top;
+        last = atomicAdd(p.ccnt + (int64_t)tok * nblk + blk, 1) == p.k_top - 1;
+    }
+    __threadfence();
+    uint32_t lm = __ballot_sync(0xffffffffu, last);
+    const int e = lane >> 3, sub = lane & 7;
+    while (lm != 0u) {
+        uint32_t m = lm;
+        for (int i = 0; i < e; ++i) m &= m - 1u;  // drop the e lowest completed tokens
+        const bool act = m != 0u;
+        const int t = __shfl_sync(0xffffffffu, tok, act ? __ffs(m) - 1 : 0);
+        if (act) {
+            float acc[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+            for (int sl = 0; sl < p.k_top; ++sl) {
+                const int r = __ldg(p.inv + (int64_t)t * p.k_top + sl);
+                const float ws = p.cw ? __ldg(p.cw + (int64_t)t * p.k_top + sl) : 1.0f;
+                const uint4 y = __ldcg(reinterpret_cast<const uint4*>(p.out + (int64_t)r * p.ldo + blk * 64 + sub * 8));
+                const uint32_t wv[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    acc[2 * j] = fmaf(ws, __uint_as_float(wv[j] << 16), acc[2 * j]);
+                    acc[2 * j + 1] = fmaf(ws, __uint_as_float(wv[j] & 0xFFFF0000u), acc[2 * j + 1]);
+                }
+            }
+            uint32_t o[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) o[j] = pack_bf16(acc[2 * j], acc[2 * j + 1]);
+            *reinterpret_cast<uint4*>(p.cout + (int64_t)t * p.N + blk * 64 + sub * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        for (int i = 0; i < 4 && lm != 0u; ++i) lm &= lm - 1u;
     }
 }
 
@@ -782,6 +841,18 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                                                                          full_warp, valid, lane, row,
                                                                          x.nt * TN + cg * C::CPW + hf * C::BOXW,
                                                                          x.row0 + q * 32);
+                if constexpr (C::COMB) {
+                    // this warp's block of Y2 is complete and visible before its rows count
+                    if (lane == 0) {
+                        bulk_wait_all();
+                        fence_proxy_async_global();
+                        __threadfence();
+                    }
+                    __syncwarp();
+                    fence_proxy_async_global();
+                    __threadfence();
+                    combine_completed(p, valid, row, (x.nt * TN + cg * C::CPW) >> 6, lane);
+                }
             } else {
                 if (valid && p.c_debug) {
                     float* cgp = p.c_debug + row * p.N + x.nt * 128 + cg * 32;
@@ -973,6 +1044,9 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
     if (qol && (g.goff == nullptr || g.d_in == nullptr || g.d_amax == nullptr || g.K % 256 != 0 ||
                 g.K / 256 > Cfg<3>::KCH || g.N % 256 != 0 || g.N / 256 < 2))
         return cudaErrorInvalidValue;
+    if (g.mode == 4 && (g.goff == nullptr || g.perm == nullptr || g.inv == nullptr || g.cout == nullptr ||
+                        g.ccnt == nullptr || g.k_top < 1 || g.K / 256 >= 4))
+        return cudaErrorInvalidValue;
     const int map_mode = g.mode == 1 ? 1 : 0;  // modes 0, 2 and 3 share the plain tensor maps
     CUtensorMap ta, tb, tsfb, to;
     const int b_rows = map_mode == 0 ? Cfg<0>::B_ROWS : Cfg<1>::B_ROWS;
@@ -1010,11 +1084,18 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
     p.q_codes = g.q_codes;
     p.q_sf = g.q_sf;
     p.q_scale = g.q_scale;
+    p.perm = g.perm;
+    p.inv = g.inv;
+    p.cw = g.cw;
+    p.cout = reinterpret_cast<__nv_bfloat16*>(g.cout);
+    p.ccnt = g.ccnt;
+    p.k_top = g.k_top;
     const int num_sms = g.num_sms > 0 ? g.num_sms : 148;
     // dense calls: no more pairs than units of work (m-tile pairs x n-tiles)
     const int tn = g.mode == 1 ? Cfg<1>::TN : Cfg<0>::TN;
     const int64_t dense_units = g.goff == nullptr ? ((g.M + BM - 1) / BM + 1) / 2 * (g.N / tn) : 0;
     if (qol) return launch_mode<3>(ta, tb, tsfb, to, p, num_sms, 0, stream);
+    if (g.mode == 4) return launch_mode<4>(ta, tb, tsfb, to, p, num_sms, 0, stream);
     if (g.mode == 0 && plain_mode == 2) return launch_mode<2>(ta, tb, tsfb, to, p, num_sms, dense_units, stream);
     if (g.mode == 0) return launch_mode<0>(ta, tb, tsfb, to, p, num_sms, dense_units, stream);
     return launch_mode<1>(ta, tb, tsfb, to, p, num_sms, dense_units, stream);

@@ -60,7 +60,7 @@ struct GemmLaunch {
     int N, K, G;
     const int* goff;       // nullable (dense: one group of M rows)
     const int* gpoff;
-    int mode;              // 0 plain, 1 SwiGLU, 3 plain with A encoded from bf16 rows in the kernel
+    int mode;              // 0 plain, 1 SwiGLU, 3 plain with A encoded from bf16 rows in the kernel, 4 plain + combine
     void* out;             // bf16
     int64_t ldo;
     float* amax_out;       // mode 1
@@ -79,6 +79,16 @@ struct GemmLaunch {
     uint8_t* q_codes;
     uint8_t* q_sf;
     float* q_scale;
+    // mode 4 (mode 0 plus the router-weighted combine in the epilogue; grouped,
+    // N a multiple of 64): perm [M] (token * k_top + slot of each row), inv
+    // [T x k_top], combine weights cw [T x k_top] (nullable: 1), the layer
+    // output cout bf16 [T x N], zeroed arrival counters ccnt [T x N/64]
+    const int* perm;
+    const int* inv;
+    const float* cw;
+    void* cout;
+    int* ccnt;
+    int k_top;
 };
 cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t stream);
 
@@ -128,6 +138,8 @@ struct RouteLaunch {
     float* a1_scale;
     float* amax2;          // zeroed here for the FC1 epilogue ([T*k])
     float* row_w;          // nullable: [T*k] router weight of each expert-ordered row
+    int* comb_cnt;         // nullable: [T x comb_blocks] arrival counters of the combine inside FC2, zeroed here
+    int comb_blocks;
 };
 constexpr int kRouteChunk = 32;  // tokens per chunk of the stable scatter (one bitmap word)
 cudaError_t launch_route(const RouteLaunch& r, cudaStream_t stream);       // top-k, then the rest

@@ -97,6 +97,11 @@ __global__ void __launch_bounds__(kThreads) route_scatter_kernel(RouteLaunch p) 
     const int nslot = kRouteChunk * k;
     const int64_t t0 = (int64_t)blockIdx.x * kRouteChunk;
     for (int i = threadIdx.x; i < E; i += kThreads) bitmap[i] = 0u;
+    if (p.comb_cnt != nullptr) {  // the combine inside FC2: this chunk's arrival counters start at zero
+        const int nb = p.comb_blocks;
+        for (int i = threadIdx.x; i < kRouteChunk * nb; i += kThreads)
+            if (t0 + i / nb < p.T) p.comb_cnt[t0 * nb + i] = 0;
+    }
     __syncthreads();
     for (int i = threadIdx.x; i < nslot; i += kThreads) {
         const int tl = i / k;

@@ -129,6 +129,10 @@ def test_moe_rejects_bad_arguments(L):
         opt.fc2_requant = bad
         assert call() == -1
     opt.fc2_requant = 0
+    for bad in (-1, 2):  # moe_options.fc2_combine is 0 or 1
+        opt.fc2_combine = bad
+        assert call() == -1
+    opt.fc2_combine = 0
 
 
 def test_quantize_grouped_rejects_bad_arguments(L):

@@ -73,16 +73,16 @@ def test_noalloc_rejects_layers_beyond_the_array():
     assert "scratch" in L.nvfp4_last_error().decode()
 
 
-def test_noalloc_boundary_is_518_tokens_at_the_qwen3_shape():
-    """The documented limit, pinned: 518 tokens fit the 32 MiB array at hidden
-    2048, FFN 768, 128 experts, top-8, and 519 are refused on the host."""
+def test_noalloc_boundary_is_516_tokens_at_the_qwen3_shape():
+    """The documented limit, pinned: 516 tokens fit the 32 MiB array at hidden
+    2048, FFN 768, 128 experts, top-8, and 517 are refused on the host."""
     L = _lib()
     limit = 32 << 20
-    assert L.moe_expert_workspace(518, H, F, E, K) <= limit < L.moe_expert_workspace(519, H, F, E, K)
+    assert L.moe_expert_workspace(516, H, F, E, K) <= limit < L.moe_expert_workspace(517, H, F, E, K)
     w1 = nv._Tensor(4096, 4096, 4096, E * 2 * F, H)
     w2 = nv._Tensor(4096, 4096, 4096, E * H, F)
     opt = nv._Options(0)
-    rc = L.moe_expert_forward_noalloc(4096, 519, H, 4096, None, E, K, ctypes.byref(w1), ctypes.byref(w2), F,
+    rc = L.moe_expert_forward_noalloc(4096, 517, H, 4096, None, E, K, ctypes.byref(w1), ctypes.byref(w2), F,
                                       ctypes.byref(opt), 4096, None)
     assert rc == -4
     assert "scratch" in L.nvfp4_last_error().decode()
