@@ -319,10 +319,11 @@ class Layer:
     """One expert layer's device inputs, pre-quantized weights, workspace and
     output, and the call that runs it."""
 
-    def __init__(self, nv, dev, d, fc2_requant=None):
+    def __init__(self, nv, dev, d, fc2_requant=None, fc2_combine=False):
         self.nv = nv
         self.d = d
         self.fc2_requant = fc2_requant
+        self.fc2_combine = fc2_combine
         self.T = d["x"].shape[0]
         self.x = torch.from_numpy(d["x"].view(np.int16)).view(torch.bfloat16).to(dev)
         self.logits = torch.from_numpy(d["logits"]).to(dev)
@@ -334,7 +335,8 @@ class Layer:
 
     def __call__(self, evs=None):
         self.nv.moe_expert_forward(self.x, self.logits, self.bias, self.w1q, self.w2q, F, K_TOP, out=self.out,
-                                   ws=self.ws, stage_events=evs, fc2_requant=self.fc2_requant)
+                                   ws=self.ws, stage_events=evs, fc2_requant=self.fc2_requant,
+                                   fc2_combine=self.fc2_combine)
 
     def check_error_word(self):
         err = self.ws[:4].view(torch.int32).item()
@@ -550,23 +552,24 @@ def moe_8k_leg(nv, local, steps, warmup):
             "eager_ms_per_step": eager_ms, "gemms_fc1_fc2": gemms, "stages": stages}
 
 
-def requant_in_fc2_leg(nv, local, steps, warmup):
-    """The 32768-token layer with the FC2 input requantized inside FC2
-    (moe_options.fc2_requant = MOE_REQUANT_IN_FC2, an option, off by
-    default): the same timing as the headline, for comparison with the
-    separate requantization launch."""
+def fused_option_leg(nv, local, steps, warmup, combine=False):
+    """The 32768-token layer with work moved into FC2, options that are off
+    by default: the FC2 input requantized inside FC2 (moe_options.fc2_requant
+    = MOE_REQUANT_IN_FC2) or, with combine, the router-weighted combine in
+    FC2's epilogue (moe_options.fc2_combine).  The same timing as the
+    headline, for comparison with the separate launches."""
     dev = torch.device("cuda", local)
-    layer = Layer(nv, dev, make_inputs(), fc2_requant="in_fc2")
+    layer = Layer(nv, dev, make_inputs(), fc2_requant=None if combine else "in_fc2", fc2_combine=combine)
     flush = L2Flush(dev)
     eager_ms, stage_ms, _, _ = time_layer(layer, steps, warmup, flush, 1, dev)
     graph, _ = graph_leg(layer, steps, flush)
     del layer
     torch.cuda.empty_cache()
     st = {s: statistics.fmean(v) for s, v in stage_ms.items()}
-    return {"workload": "moe_expert_layer_32k, FC2 input requantized inside FC2 (GEMM mode 3)",
+    what = "combine in FC2's epilogue (GEMM mode 4)" if combine else "FC2 input requantized inside FC2 (GEMM mode 3)"
+    return {"workload": "moe_expert_layer_32k, " + what,
             "ms_per_step": graph["ms_per_step"], "tokens_per_s": T / (graph["ms_per_step"] / 1e3),
-            "eager_ms_per_step": eager_ms, "fc2_with_requant_ms": st["fc2"], "requant_stage_ms": st["requant"],
-            "stages_ms": st}
+            "eager_ms_per_step": eager_ms, "fc2_ms": st["fc2"], "stages_ms": st}
 
 
 def _graph_per_launch(calls, replays, dev):
@@ -1086,6 +1089,8 @@ def summary_of(res):
         out["moe_8k_fc1_plus_fc2_frac_of_9pf"] = res["moe_8k"]["gemms_fc1_fc2"]["frac_of_9pf"]
     if res.get("requant_in_fc2"):
         out["moe_32k_requant_in_fc2_tokens_per_s"] = res["requant_in_fc2"]["tokens_per_s"]
+    if res.get("combine_in_fc2"):
+        out["moe_32k_combine_in_fc2_tokens_per_s"] = res["combine_in_fc2"]["tokens_per_s"]
     if res.get("sustained"):
         su = res["sustained"]
         out["sustained_tokens_per_s"] = su["tokens_per_s"]
@@ -1137,7 +1142,8 @@ def main():
             del layer
             torch.cuda.empty_cache()
             res["moe_8k"] = moe_8k_leg(nv, local, args.steps, args.warmup)
-            res["requant_in_fc2"] = requant_in_fc2_leg(nv, local, args.steps, args.warmup)
+            res["requant_in_fc2"] = fused_option_leg(nv, local, args.steps, args.warmup)
+            res["combine_in_fc2"] = fused_option_leg(nv, local, args.steps, args.warmup, combine=True)
             res["quant"] = quant_gbs(args, local)
             res["quant_four_over_six"] = quant_gbs(args, local, four_over_six="mse")
             res["dequant"] = dequant_gbs(args, local)
