@@ -47,7 +47,9 @@
 //                through a per-warp shared-memory box and a TMA tensor store;
 //                a warp whose 32 rows straddle the end of an expert group
 //                stores its valid rows directly.  In mode 3 these warps also
-//                encode the resident A tile (and warp 0 has no role).
+//                encode the resident A tile (and warp 0 has no role); in
+//                mode 4 they also sum the router-weighted combine of the
+//                tokens whose last row they write.
 // Work units are (pair of m-tiles of one group, n-tile), n fastest, so pairs
 // running at the same time share the A rows and one expert's weights in L2.
 // A group with an odd number of m-tiles ends in a unit whose odd CTA has no
@@ -102,6 +104,8 @@ constexpr int MAX_G = 256;
 // (codes in the MMA's swizzled layout, block scales as atoms) and the row
 // scales; a pair then runs all n-tiles of its m-tiles back to back on that
 // tile.  B streams through the 4-stage ring as in mode 0.
+// Mode 4 is mode 0 with the expert layer's router-weighted combine in the
+// epilogue (combine_completed below).
 template <int MODE>
 struct Cfg {
     static constexpr int BK = 256;                      // FP4 elements of K per stage
