@@ -75,6 +75,9 @@ constexpr int EPI_WARP0 = 6;            // warps 2..5 write scales, 6..21 run th
 constexpr int EPI_WARPS = 16;
 constexpr int PRODB_WARP = EPI_WARP0 + EPI_WARPS;  // warp 22: producer of B
 constexpr int THREADS = (PRODB_WARP + 1) * 32;
+constexpr int ISSUE2_WARP = PRODB_WARP + 1;          // mode 5: warp 23 issues the second half's MMAs
+template <int MODE>
+constexpr int threads_of() { return MODE == 5 ? (ISSUE2_WARP + 1) * 32 : THREADS; }
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;
 constexpr uint32_t SF_COL = 256;
@@ -117,7 +120,11 @@ struct Cfg {
     static constexpr bool PLAIN = MODE != 1;            // modes 0, 2 and 3: plain bf16 out
     static constexpr bool QOL = MODE == 3;              // A quantized on load, resident across n-tiles
     static constexpr bool COMB = MODE == 4;             // mode 0 plus the combine in the epilogue
-    static constexpr int STAGES = (MODE == 0 || MODE == 3 || MODE == 4) ? 4 : 5;
+    // mode 5: mode 0 with two MMA issuers, one per 128-column half of the
+    // tile, each with its own accumulator and hand-off
+    static constexpr bool DUAL = MODE == 5;
+    static constexpr int NACC = DUAL ? 2 : 1;           // accumulator barriers (ACC_BUFS is 1 in every mode)
+    static constexpr int STAGES = (MODE == 0 || MODE == 3 || MODE == 4 || MODE == 5) ? 4 : 5;
     static constexpr int KCH = 3;                       // mode 3: K-stages of the resident A tile (K <= 768)
     static constexpr int A_SLOTS = QOL ? KCH : STAGES;  // A slots: the ring, or the resident tile's stages
     static constexpr int NBUF = 1;                      // staging boxes per epilogue warp
@@ -129,9 +136,9 @@ struct Cfg {
     static constexpr int SWZ = 2;                       // descriptor swizzle code: 128B
     static constexpr int SBO = 8 * ROWB;                // bytes between 8-row core-matrix groups
     static constexpr uint32_t SF_STAGE_COLS = 4 * ATOMS * (1 + SFB_BLOCKS);  // SFA 4 + SFB 4 per block, per atom
-    static constexpr uint32_t IDESC = idesc_nvfp4(2 * BM, TN);
+    static constexpr uint32_t IDESC = idesc_nvfp4(2 * BM, DUAL ? TN / 2 : TN);
     static constexpr int CPW = PLAIN ? TN / 4 : 32;       // output columns per epilogue warp per tile
-    static constexpr int BOXW = (MODE == 0 || MODE == 3 || MODE == 4) ? CPW : 32;  // store box width (columns)
+    static constexpr int BOXW = (MODE == 0 || MODE == 3 || MODE == 4 || MODE == 5) ? CPW : 32;  // store box width (columns)
     static constexpr int STG_BYTES = 32 * BOXW * 2;       // one staging box: 32 rows x BOXW bf16
     static constexpr bool STAGED = true;
     static constexpr bool TMA_STORE = true;               // false: coalesced warp stores from the staging box
@@ -152,8 +159,8 @@ struct __align__(1024) Smem {
     uint64_t full_b[C::STAGES];    // this CTA's B half and the weight scales landed
     uint64_t sf_full[C::STAGES];   // (even CTA) scales of the stage in TMEM: 4 warps of each CTA
     uint64_t empty[C::STAGES];     // MMAs of the stage done (commit, multicast to the pair)
-    uint64_t tmem_full[C::ACC_BUFS];   // accumulator ready (commit, multicast to the pair)
-    uint64_t tmem_empty[C::ACC_BUFS];  // (even CTA) accumulator drained: one arrival per epilogue warp of the pair
+    uint64_t tmem_full[C::NACC];   // accumulator ready (commit, multicast to the pair)
+    uint64_t tmem_empty[C::NACC];  // (even CTA) accumulator drained: one arrival per epilogue warp of the pair
     uint64_t a_full[C::A_SLOTS];   // mode 3: K-stage of the resident A tile encoded (one arrival per epilogue warp)
     uint64_t drain;
     uint64_t never;                // no arrival ever: the time-out test's wait
@@ -166,7 +173,7 @@ struct __align__(1024) Smem {
 };
 static_assert(sizeof(Smem<0>) + 1024 <= 232448 && sizeof(Smem<1>) + 1024 <= 232448 &&
               sizeof(Smem<2>) + 1024 <= 232448 && sizeof(Smem<3>) + 1024 <= 232448 &&
-              sizeof(Smem<4>) + 1024 <= 232448, "shared memory per CTA");
+              sizeof(Smem<4>) + 1024 <= 232448 && sizeof(Smem<5>) + 1024 <= 232448, "shared memory per CTA");
 // the two plain forms share the host-side tensor maps
 static_assert(Cfg<2>::ROWB == Cfg<0>::ROWB && Cfg<2>::ATOMS == Cfg<0>::ATOMS && Cfg<2>::TN == Cfg<0>::TN &&
               Cfg<2>::B_ROWS == Cfg<0>::B_ROWS && Cfg<2>::SFB_BLOCKS == Cfg<0>::SFB_BLOCKS, "plain forms");
@@ -507,7 +514,7 @@ __device__ __forceinline__ void prefetch_a_rows(const KParams& p, int row0, int 
 }
 
 template <int MODE>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<MODE>(), 1)
 gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ CUtensorMap tmSFB, const __grid_constant__ CUtensorMap tmO,
                   const KParams p) {
@@ -530,22 +537,23 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             s.gpoff[0] = 0; s.gpoff[1] = (int)((p.M + BM - 1) / BM * BM);
         }
     } else {
-        for (int i = threadIdx.x; i <= G; i += THREADS) { s.goff[i] = p.goff[i]; s.gpoff[i] = p.gpoff[i]; }
+        for (int i = threadIdx.x; i <= G; i += threads_of<MODE>()) { s.goff[i] = p.goff[i]; s.gpoff[i] = p.gpoff[i]; }
     }
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
             mbar_init(smem_u32(&s.full_a[i]), 1);
             mbar_init(smem_u32(&s.full_b[i]), 1);
             mbar_init(smem_u32(&s.sf_full[i]), 8);
-            mbar_init(smem_u32(&s.empty[i]), 1);
+            mbar_init(smem_u32(&s.empty[i]), C::DUAL ? 2 : 1);  // mode 5: a commit from each issuer
         }
-        for (int i = 0; i < ACC_BUFS; ++i) {
+        for (int i = 0; i < C::NACC; ++i) {
             mbar_init(smem_u32(&s.tmem_full[i]), 1);
-            mbar_init(smem_u32(&s.tmem_empty[i]), 2 * EPI_WARPS);
+            // the epilogue warps of the pair that drain this accumulator (mode 5: half of them)
+            mbar_init(smem_u32(&s.tmem_empty[i]), C::DUAL ? EPI_WARPS : 2 * EPI_WARPS);
         }
         if (C::QOL)
             for (int i = 0; i < C::A_SLOTS; ++i) mbar_init(smem_u32(&s.a_full[i]), EPI_WARPS);
-        mbar_init(smem_u32(&s.drain), 1);
+        mbar_init(smem_u32(&s.drain), C::DUAL ? 2 : 1);
         mbar_init(smem_u32(&s.never), 1);
         s.abort = 0;
         fence_barrier_init();
@@ -628,7 +636,15 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     } else {
                         // the scale box is always whole: atoms past K are zero-filled
                         mbar_arrive_expect_tx(fb, B_BYTES + SFB_BYTES);
-                        tma_load_2d(smem_u32(s.b[stage]), &tmB, fb, ks * ROWB, brow);
+                        if constexpr (C::DUAL) {
+                            // half h of the tile (its 128 weight rows) is split between the pair:
+                            // this CTA stages rows h * 128 + rank * 64 .. + 63 at b + h * (B_BYTES / 2)
+                            tma_load_2d(smem_u32(s.b[stage]), &tmB, fb, ks * ROWB, jb0 * 128 + (int)rank * 64);
+                            tma_load_2d(smem_u32(s.b[stage]) + B_BYTES / 2, &tmB, fb, ks * ROWB,
+                                        jb0 * 128 + 128 + (int)rank * 64);
+                        } else {
+                            tma_load_2d(smem_u32(s.b[stage]), &tmB, fb, ks * ROWB, brow);
+                        }
                         if (MODE == 1)
                             tma_load_4d(smem_u32(s.sfb[stage]), &tmSFB, fb, 0, ks * ATOMS, x.nt, 2 * x.g);
                         else
@@ -647,9 +663,13 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 }
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || (C::DUAL && warp == ISSUE2_WARP)) {
         if (lane == 0 && rank == 0) {
             // ------------------------------------------------------------ MMA issuer (even CTA)
+            // Mode 5 has two: warp 1 issues the MMAs of the tile's first 128
+            // columns into accumulator 0, warp 23 those of the last 128 into
+            // accumulator 1 (N = 128 each; both read the same A stage, each its
+            // half of B, and both commit on the stage's empty barrier).
             // The issuing thread's instruction stream is kept short (it shares
             // its scheduler with epilogue warps): descriptors of stage 0 are
             // built once, a stage / K-step adds its byte offset >> 4 to the
@@ -657,16 +677,17 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             // sf_full alone suffices: this CTA's scale writers arrive on it
             // only after both of its stage's copies have landed, the peer's
             // after the peer's have.
+            const int hh = (C::DUAL && warp == ISSUE2_WARP) ? 1 : 0;  // mode 5: the half this thread issues
             const uint64_t adesc0 = smem_desc(smem_u32(s.a[0]), 0, SBO, SWZ);
-            const uint64_t bdesc0 = smem_desc(smem_u32(s.b[0]), 0, SBO, SWZ);
+            const uint64_t bdesc0 = smem_desc(smem_u32(s.b[0]) + (C::DUAL ? hh * (B_BYTES / 2) : 0), 0, SBO, SWZ);
             int stage = 0, it = 0;
             uint32_t phase = 0;
             bool ok = true;
             // the time-out test: a bounded wait for a phase that never completes
-            if (p.stall) ok = mbar_wait_bounded_relaxed(smem_u32(&s.never), 0, abort, p.err);
+            if (p.stall && hh == 0) ok = mbar_wait_bounded_relaxed(smem_u32(&s.never), 0, abort, p.err);
             for (int u = u_first; u < total && ok; u = u_next(u), ++it) {
-                // accumulator it % ACC_BUFS, in its (it / ACC_BUFS)-th use
-                const int ab = ACC_BUFS == 1 ? 0 : (it & 1);
+                // accumulator it % ACC_BUFS, in its (it / ACC_BUFS)-th use; mode 5: this half's
+                const int ab = C::DUAL ? hh : (ACC_BUFS == 1 ? 0 : (it & 1));
                 const uint32_t acc_phase = (uint32_t)(ACC_BUFS == 1 ? it : it >> 1) & 1u;
                 if (!mbar_wait_bounded_relaxed(smem_u32(&s.tmem_empty[ab]), acc_phase ^ 1, abort, p.err)) { ok = false; break; }
                 tc_fence_after();
@@ -679,9 +700,15 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     const uint64_t bd = bdesc0 + (uint64_t)((stage * B_BYTES) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < ATOMS; ++kk) {
-                        if (kk < na)
-                            tc_mma2_nvfp4(tmem + ACC_COL + ab * TN, ad + 2 * kk, bd + 2 * kk, C::IDESC, sfc + kk * 4,
-                                          sfc + 4 * ATOMS + kk * 4 * SFB_BLOCKS, (ks | kk) != 0);
+                        if (kk < na) {
+                            if constexpr (C::DUAL)  // half hh: 128 accumulator columns, its 128-row weight-scale block
+                                tc_mma2_nvfp4(tmem + ACC_COL + hh * (TN / 2), ad + 2 * kk, bd + 2 * kk, C::IDESC,
+                                              sfc + kk * 4, sfc + 4 * ATOMS + kk * 4 * SFB_BLOCKS + 4 * hh,
+                                              (ks | kk) != 0);
+                            else
+                                tc_mma2_nvfp4(tmem + ACC_COL + ab * TN, ad + 2 * kk, bd + 2 * kk, C::IDESC,
+                                              sfc + kk * 4, sfc + 4 * ATOMS + kk * 4 * SFB_BLOCKS, (ks | kk) != 0);
+                        }
                     }
                     tc_commit2_mc(smem_u32(&s.empty[stage]), 3);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -767,7 +794,8 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             }
         }
         for (int u = u_first; u < total; u = u_next(u), ++it) {
-            const int ab = ACC_BUFS == 1 ? 0 : (it & 1);
+            // mode 5: column groups 0-1 drain accumulator 0 (the tile's first 128 columns), 2-3 accumulator 1
+            const int ab = C::DUAL ? (cg >> 1) : (ACC_BUFS == 1 ? 0 : (it & 1));
             const uint32_t acc_phase = (uint32_t)(ACC_BUFS == 1 ? it : it >> 1) & 1u;
             const Tile x = decode_unit(s, G, n_tiles, u, rank);
             const int rl = q * 32 + lane;
@@ -797,7 +825,8 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             uint32_t v[C::PLAIN ? C::CPW : 64];
             if (C::PLAIN) {
 #pragma unroll
-                for (int h = 0; h < C::CPW / 32; ++h) tmem_ld32(lane_addr + ACC_COL + ab * TN + cg * C::CPW + 32 * h, v + 32 * h);
+                for (int h = 0; h < C::CPW / 32; ++h)
+                    tmem_ld32(lane_addr + ACC_COL + (C::DUAL ? 0 : ab * TN) + cg * C::CPW + 32 * h, v + 32 * h);
             } else {
                 tmem_ld32(lane_addr + ACC_COL + cg * 32, v);             // gate
                 tmem_ld32(lane_addr + ACC_COL + 128 + cg * 32, v + 32);  // up
@@ -985,7 +1014,7 @@ template <int MODE>
 int resident_pairs(size_t smem, int num_sms) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(num_sms & ~1), 1, 1);
-    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.blockDim = dim3(threads_of<MODE>(), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -1026,7 +1055,7 @@ cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
     }
     if (dense_units > 0 && dense_units < pairs) pairs = (int)dense_units;
     if (pairs < 1) pairs = 1;
-    gemm_nvfp4_kernel<MODE><<<2 * pairs, THREADS, smem, stream>>>(ta, tb, tsfb, to, p);
+    gemm_nvfp4_kernel<MODE><<<2 * pairs, threads_of<MODE>(), smem, stream>>>(ta, tb, tsfb, to, p);
     return cudaGetLastError();
 }
 
@@ -1053,9 +1082,12 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
         return cudaErrorInvalidValue;
     const int map_mode = g.mode == 1 ? 1 : 0;  // modes 0, 2 and 3 share the plain tensor maps
     CUtensorMap ta, tb, tsfb, to;
-    const int b_rows = map_mode == 0 ? Cfg<0>::B_ROWS : Cfg<1>::B_ROWS;
-    // plain GEMMs with long K loops (4 or more stages of 256) take the 5-stage form
-    const int plain_mode = (g.K / 256 >= 4) ? 2 : 0;
+    // plain GEMMs with long K loops (4 or more stages of 256) take the 5-stage form;
+    // shorter ones the two-issuer form (mode 5)
+    const int plain_mode = (g.K / 256 >= 4) ? 2 : 5;
+    const bool dual = g.mode == 0 && plain_mode == 5;
+    // mode 5 stages each half of a CTA's weight rows as its own 64-row box
+    const int b_rows = dual ? Cfg<5>::B_ROWS / 2 : (map_mode == 0 ? Cfg<0>::B_ROWS : Cfg<1>::B_ROWS);
     if (!make_codes_map(&tb, g.b_codes, (int64_t)g.G * g.N, g.K / 2, map_mode, b_rows)) return cudaErrorInvalidValue;
     // mode 3 has no A tensor (the kernel encodes A): its map argument repeats B's, unused
     if (qol) ta = tb;
@@ -1101,6 +1133,7 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
     if (qol) return launch_mode<3>(ta, tb, tsfb, to, p, num_sms, 0, stream);
     if (g.mode == 4) return launch_mode<4>(ta, tb, tsfb, to, p, num_sms, 0, stream);
     if (g.mode == 0 && plain_mode == 2) return launch_mode<2>(ta, tb, tsfb, to, p, num_sms, dense_units, stream);
+    if (dual) return launch_mode<5>(ta, tb, tsfb, to, p, num_sms, dense_units, stream);
     if (g.mode == 0) return launch_mode<0>(ta, tb, tsfb, to, p, num_sms, dense_units, stream);
     return launch_mode<1>(ta, tb, tsfb, to, p, num_sms, dense_units, stream);
 }
