@@ -319,12 +319,16 @@ def test_moe_qwen3_shapes_stagewise(name):
     check_stagewise(d, E, k, F, dev, experts=experts, token_sample=toks)
 
 
-def test_moe_router_ties_and_signed_zeros():
+@pytest.mark.parametrize("E,k", [(128, 8), (96, 6), (256, 16), (32, 4), (160, 9)])
+def test_moe_router_ties_and_signed_zeros(E, k):
     """Logits from a handful of values (exact ties everywhere, +0 and -0
-    among them) through the 128-expert layer whose top-k shares a launch with
-    the quantization of X: ids must match the oracle's lower-index tie rule
-    exactly (-0 and +0 are one value), and the rest of the layer with it."""
-    T, E, k, H, F = 512, 128, 8, 1024, 128
+    among them): ids must match the oracle's lower-index tie rule exactly
+    (-0 and +0 are one value), and the rest of the layer with it.  E = 128
+    runs the top-k that shares a launch with the quantization of X; the
+    others the top-k launched alone, with 1, 3, 5 and 8 logits per lane (a
+    lane's keys are sorted before the rounds, so equal keys inside one lane
+    must keep their expert order)."""
+    T, H, F = 512, 1024, 128
     rng = np.random.default_rng(17)
     d = small_layer(T, E, k, H, F, seed=17)
     vals = np.array([-1.0, -0.0, 0.0, 0.5, 1.0, 2.0], np.float32)
