@@ -423,6 +423,7 @@ int moe_expert_forward(const void* x_bf16, int64_t T, int64_t H, const float* ro
     qx.sf = at(L.xq_sf);
     qx.sf_ld = H / 16;  // row-linear: the permute gathers whole rows of scales
     qx.fos = fos;
+    qx.x_once = 1;  // X leaves L2 first: its codes stay there for the permute's 8 reads of each row
     qx.scale = reinterpret_cast<float*>(at(L.xq_scale));
     qx.err = reinterpret_cast<uint32_t*>(at(L.err));
 

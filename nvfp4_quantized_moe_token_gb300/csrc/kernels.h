@@ -21,6 +21,8 @@ struct QuantLaunch {
     int G;
     int reverse;            // rows taken last to first
     int fos;                // four-over-six: 0 off, 1 by MSE, 2 by MAE
+    int x_once;             // the rows are read once: their L2 lines are marked evict-first, so
+                            // that they do not push the outputs out of L2 before the next kernel
     int groups;             // per_tensor: one outer scale per group of rows / groups rows (0 or 1: one)
     void* ws;               // >= 16 + 4 * groups bytes when per_tensor && !amax_in
     uint32_t* err;          // nullable device error word (pipeline wait time-outs)
