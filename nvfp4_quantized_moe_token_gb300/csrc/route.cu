@@ -64,13 +64,35 @@ __global__ void __launch_bounds__(kThreads) route_scan_kernel(RouteLaunch p, int
     const int e = blockIdx.x;
     const int per = (nchunks + kThreads - 1) / kThreads;
     const int c0 = threadIdx.x * per;
+    // up to kScanRegs chunks per thread (T <= 65536 tokens): the counts are
+    // loaded once, all in flight together, and kept in registers for the bases
+    constexpr int kScanRegs = 8;
+    int v[kScanRegs];
     int local = 0;
-    for (int c = c0; c < c0 + per && c < nchunks; ++c) local += p.chunk_cnt[(int64_t)c * E + e];
+    if (per <= kScanRegs) {
+#pragma unroll
+        for (int j = 0; j < kScanRegs; ++j)
+            v[j] = (j < per && c0 + j < nchunks) ? p.chunk_cnt[(int64_t)(c0 + j) * E + e] : 0;
+#pragma unroll
+        for (int j = 0; j < kScanRegs; ++j) local += v[j];
+    } else {
+        for (int c = c0; c < c0 + per && c < nchunks; ++c) local += p.chunk_cnt[(int64_t)c * E + e];
+    }
     int total;
     int base = block_exclusive_scan(local, &total);
-    for (int c = c0; c < c0 + per && c < nchunks; ++c) {
-        p.chunk_base[(int64_t)c * E + e] = base;
-        base += p.chunk_cnt[(int64_t)c * E + e];
+    if (per <= kScanRegs) {
+#pragma unroll
+        for (int j = 0; j < kScanRegs; ++j) {
+            if (j < per && c0 + j < nchunks) {
+                p.chunk_base[(int64_t)(c0 + j) * E + e] = base;
+                base += v[j];
+            }
+        }
+    } else {
+        for (int c = c0; c < c0 + per && c < nchunks; ++c) {
+            p.chunk_base[(int64_t)c * E + e] = base;
+            base += p.chunk_cnt[(int64_t)c * E + e];
+        }
     }
     __shared__ int is_last;
     if (threadIdx.x == 0) {
@@ -102,23 +124,34 @@ __global__ void __launch_bounds__(kThreads) route_scatter_kernel(RouteLaunch p) 
         for (int i = threadIdx.x; i < kRouteChunk * nb; i += kThreads)
             if (t0 + i / nb < p.T) p.comb_cnt[t0 * nb + i] = 0;
     }
-    __syncthreads();
-    for (int i = threadIdx.x; i < nslot; i += kThreads) {
-        const int tl = i / k;
-        if (t0 + tl >= p.T) continue;
-        const int e = p.ids[t0 * k + i];
-        if (e < 0 || e >= E) atomicOr(p.err, NVFP4_DEVERR_BADEXPERT);
-        else atomicOr(&bitmap[e], 1u << tl);
+    // each thread's slots (32 tokens x k <= 16 slots over 256 threads: at most 2),
+    // their experts and their rows' first positions are loaded once, before the
+    // bitmap is complete
+    constexpr int kSlotRegs = kRouteChunk * 16 / kThreads;
+    static_assert(kSlotRegs * kThreads >= kRouteChunk * 16, "slots per thread");
+    int ev[kSlotRegs], base[kSlotRegs];
+#pragma unroll
+    for (int j = 0; j < kSlotRegs; ++j) {
+        const int i = threadIdx.x + j * kThreads;
+        const bool in = i < nslot && t0 + i / k < p.T;
+        ev[j] = in ? p.ids[t0 * k + i] : -1;
+        const bool good = ev[j] >= 0 && ev[j] < E;
+        if (in && !good) ev[j] = -1;
+        base[j] = good ? __ldg(p.off + ev[j]) + p.chunk_base[(int64_t)blockIdx.x * E + ev[j]] : 0;
+        if (in && !good) atomicOr(p.err, NVFP4_DEVERR_BADEXPERT);
     }
+    __syncthreads();  // the bitmap is zeroed
+#pragma unroll
+    for (int j = 0; j < kSlotRegs; ++j)
+        if (ev[j] >= 0) atomicOr(&bitmap[ev[j]], 1u << ((threadIdx.x + j * kThreads) / k));
     __syncthreads();
-    for (int i = threadIdx.x; i < nslot; i += kThreads) {
+#pragma unroll
+    for (int j = 0; j < kSlotRegs; ++j) {
+        if (ev[j] < 0) continue;
+        const int i = threadIdx.x + j * kThreads;
         const int tl = i / k;
-        if (t0 + tl >= p.T) continue;
         const int64_t ts = t0 * k + i;  // = t * k + slot
-        const int e = p.ids[ts];
-        if (e < 0 || e >= E) continue;
-        const int rank = __popc(bitmap[e] & ((1u << tl) - 1u));
-        const int pos = __ldg(p.off + e) + p.chunk_base[(int64_t)blockIdx.x * E + e] + rank;
+        const int pos = base[j] + __popc(bitmap[ev[j]] & ((1u << tl) - 1u));
         p.perm[pos] = (int)ts;
         p.inv[ts] = pos;
         p.amax2[pos] = 0.0f;
