@@ -21,6 +21,8 @@
 //   4. route_permute: one block per padded 128-row m-tile of an expert copies
 //      its rows' codes, block scales (staged in shared memory, written as
 //      whole swizzled atoms) and outer scales into the expert-ordered buffers.
+#include <climits>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "route_topk.cuh"
@@ -176,15 +178,17 @@ __global__ void __launch_bounds__(kThreads) route_permute_kernel(RouteLaunch p) 
     // tiles last to first: FC1 reads them first to last, and finds the ones
     // written last still in L2
     const int E = p.E;
-    const int n_tiles = __ldg(p.poff + E) / kTileRows;
-    if ((int)blockIdx.x >= n_tiles) return;
+    // the expert whose padded rows hold the tile: the number of expert starts
+    // poff[1 .. E-1] at or below its first row, one per thread (E <= 256), all
+    // loaded together with the total
+    const int ptotal = __ldg(p.poff + E);
+    const int pstart = (int)threadIdx.x + 1 < E ? __ldg(p.poff + threadIdx.x + 1) : INT_MAX;
+    const int n_tiles = ptotal / kTileRows;
+    if ((int)blockIdx.x >= n_tiles) return;  // block-uniform
     const int tile = n_tiles - 1 - (int)blockIdx.x;
     const int prow0 = tile * kTileRows;
-    int lo = 0, hi = E;  // the expert whose padded rows hold prow0
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (__ldg(p.poff + mid) <= prow0) lo = mid; else hi = mid;
-    }
+    static_assert(kThreads >= 255, "one expert start per thread");
+    const int lo = __syncthreads_count(pstart <= prow0);
     const int pos0 = __ldg(p.off + lo) + (prow0 - __ldg(p.poff + lo));
     const int end = __ldg(p.off + lo + 1);
     const int nrows = end - pos0 < kTileRows ? end - pos0 : kTileRows;
