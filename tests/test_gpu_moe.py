@@ -301,6 +301,19 @@ def _pick_experts(m, n_random, seed):
     return sorted(pick)
 
 
+def test_moe_long_layer_past_the_scan_register_form():
+    """70000 tokens: 2188 routing chunks, more than the 8 per thread that the
+    scan keeps in registers, so it takes its loop form; top-2 of 32 experts
+    (the top-k launched alone). Routing metadata, permute and requant exact,
+    the GEMMs and the combine within tolerance, as in the other layers."""
+    T, E, k, H, F = 70000, 32, 2, 256, 128
+    d = small_layer(T, E, k, H, F, seed=70)
+    dev = run_device(d, E, k, F)
+    m = oracle.route_metadata(oracle.route(d["logits"], d["bias"], k)[0], E)
+    toks = np.random.default_rng(3).choice(T, 2048, replace=False)
+    check_stagewise(d, E, k, F, dev, experts=_pick_experts(m, 2, 2), token_sample=toks)
+
+
 @pytest.mark.parametrize("name", ["moe_8k", "moe_32k"])
 def test_moe_qwen3_shapes_stagewise(name):
     """8192 tokens (bias ~N(0,1)) and 32768 tokens (bias ~N(0,4): empty and
