@@ -416,12 +416,26 @@ NVFP4_API int moe_expert_forward(const void* x_bf16, int64_t T, int64_t H,
  *   All calls on a device share the one array: calls whose work overlaps on
  *   the GPU (different streams without ordering) race and corrupt each
  *   other.  Each call clears the device error word at the start of the
- *   array; device-side error bits are not reported to the caller.
+ *   array; moe_noalloc_error_word() gives its address, so that the caller
+ *   can read the call's device-side error bits in stream order.
  */
 NVFP4_API int moe_expert_forward_noalloc(const void* x_bf16, int64_t T, int64_t H,
                                          const float* router_logits, const float* router_bias, int E,
                                          int topk, const nvfp4_tensor* w1, const nvfp4_tensor* w2,
                                          int64_t F, const moe_options* opt, void* out_bf16, void* stream);
+
+/*
+ * moe_noalloc_error_word: *out = the device address, on the current device,
+ * of moe_expert_forward_noalloc's device error word (a uint32 at the start
+ * of its built-in array; bits NVFP4_DEVERR_*).  Each no-alloc call clears it
+ * before its kernels run; read it after the call in the call's stream order
+ * (for example a 4-byte cudaMemcpyAsync on the same stream, then a
+ * synchronize).  The address stays valid for the life of the process, with
+ * the same caveat as the entry point (no use after a device reset).
+ * Returns NVFP4_OK, NVFP4_EINVAL for a null out, NVFP4_ELAUNCH without a
+ * usable current device.
+ */
+NVFP4_API int moe_noalloc_error_word(uint32_t** out);
 
 /* Message describing the last error returned on the calling thread ("" if none). */
 NVFP4_API const char* nvfp4_last_error(void);

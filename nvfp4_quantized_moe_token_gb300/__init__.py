@@ -58,7 +58,7 @@ SYMBOLS = ["nvfp4_sf_bytes", "nvfp4_quantize_workspace", "nvfp4_quantize_rows", 
            "nvfp4_dequantize_rows",
            "nvfp4_linear", "nvfp4_grouped_dgrad_bf16", "nvfp4_grouped_wgrad_bf16",
            "moe_expert_workspace_layout", "moe_expert_workspace", "moe_expert_forward",
-           "moe_expert_forward_noalloc", "nvfp4_last_error"]
+           "moe_expert_forward_noalloc", "moe_noalloc_error_word", "nvfp4_last_error"]
 
 
 class NVFP4Error(RuntimeError):

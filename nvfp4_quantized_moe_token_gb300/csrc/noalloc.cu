@@ -85,4 +85,15 @@ NVFP4_API int moe_expert_forward_noalloc(const void* x_bf16, int64_t T, int64_t 
                               nullptr, ws, kScratchBytes, stream);
 }
 
+NVFP4_API int moe_noalloc_error_word(uint32_t** out) {
+    if (out == nullptr) return nvfp4::set_last_error(NVFP4_EINVAL, "moe_noalloc_error_word: null out");
+    void* ws = nullptr;
+    const int rc = scratch_address(&ws);
+    if (rc != NVFP4_OK) return rc;
+    moe_workspace_layout layout;  // the error word's offset in any layer's workspace (the first field)
+    if (moe_expert_workspace_layout(1, 256, 128, 32, 1, &layout) != NVFP4_OK) return NVFP4_ELAUNCH;
+    *out = reinterpret_cast<uint32_t*>(static_cast<unsigned char*>(ws) + layout.err);
+    return NVFP4_OK;
+}
+
 }  // extern "C"

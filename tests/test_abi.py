@@ -133,6 +133,9 @@ def test_moe_rejects_bad_arguments(L):
         opt.fc2_combine = bad
         assert call() == -1
     opt.fc2_combine = 0
+    # the no-alloc error word's accessor refuses a null out before touching a device
+    L.moe_noalloc_error_word.argtypes = [ctypes.c_void_p]
+    assert L.moe_noalloc_error_word(None) == -1
 
 
 def test_quantize_grouped_rejects_bad_arguments(L):

@@ -86,3 +86,39 @@ def test_noalloc_boundary_is_516_tokens_at_the_qwen3_shape():
                                       ctypes.byref(opt), 4096, None)
     assert rc == -4
     assert "scratch" in L.nvfp4_last_error().decode()
+
+
+class _DevWord:
+    """A uint32 at a raw device address, for torch.as_tensor (CUDA array interface)."""
+
+    def __init__(self, ptr):
+        self.__cuda_array_interface__ = {"shape": (1,), "typestr": "<u4", "data": (ptr, False), "version": 3}
+
+
+@pytest.mark.gpu
+def test_noalloc_error_word_is_the_calls_own_and_clear_after_a_good_call():
+    """moe_noalloc_error_word gives the device address of the word the
+    no-alloc call clears and its kernels set: poisoned before a good call,
+    it reads zero after it."""
+    L = _lib()
+    f = L.moe_noalloc_error_word
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.POINTER(ctypes.c_void_p)]
+    assert f(None) == -1  # NVFP4_EINVAL for a null out
+    ptr = ctypes.c_void_p()
+    assert f(ctypes.byref(ptr)) == 0 and ptr.value
+    word = torch.as_tensor(_DevWord(ptr.value), device="cuda")
+    word.fill_(0x7FFFFFFF)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(23)
+    w1q = nv.quantize_grouped_weights(to_dev_bf16(workloads.gaussian_bf16(rng, (E, 2 * F, H), std=0.02)))
+    w2q = nv.quantize_grouped_weights(to_dev_bf16(workloads.gaussian_bf16(rng, (E, H, F), std=0.02)))
+    x = to_dev_bf16(workloads.gaussian_bf16(rng, (T, H)))
+    logits = torch.from_numpy(rng.standard_normal((T, E), dtype=np.float32)).cuda()
+    bias = torch.zeros(E, dtype=torch.float32, device="cuda")
+    out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    _noalloc(L, x, logits, bias, w1q, w2q, out)
+    torch.cuda.synchronize()
+    assert int(word.item()) == 0
+    ptr2 = ctypes.c_void_p()
+    assert f(ctypes.byref(ptr2)) == 0 and ptr2.value == ptr.value  # one address for the process
